@@ -1,0 +1,47 @@
+"""exact_attention_67_gb300 -- fused exact attention for NVIDIA GB300 (sm_103a).
+
+O = softmax(scale * Q K^T [+ causal mask]) V in one fused TMA + tcgen05 kernel
+with an online softmax (S and P never leave the chip), and its gradient with
+tile-by-tile recomputation from the stored logsumexp.  The C ABI is in
+``include/exattn.h``; ``attn_fwd`` / ``attn_bwd`` here are its ctypes binding
+(same names, argument marshalling only) and :func:`forward` /
+:func:`backward` allocate the outputs with PyTorch.
+"""
+from __future__ import annotations
+
+import math
+
+from ._lib import (EXPORTS, ExattnError, attn_bwd, attn_bwd_workspace_size, attn_fwd, device_error,
+                   library_path, load, status_string, version)
+
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "forward", "backward", "device_error",
+           "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
+
+
+def _default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate O (bf16) and lse (fp32) with torch and run ``attn_fwd``."""
+    import torch
+    B, H, N, d = q.shape
+    s = _default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, causal, s, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, stream=None,
+             workspace=None):
+    """Allocate dQ, dK, dV (and the workspace unless given) and run ``attn_bwd``."""
+    import torch
+    B, H, N, d = q.shape
+    s = _default_scale(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        nbytes = attn_bwd_workspace_size(B, H, N, d, causal)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
+    return dq, dk, dv

@@ -1,0 +1,145 @@
+"""ctypes binding of libexattn.so: the C ABI of include/exattn.h under the
+same names, argument marshalling only.  Every step of the computation runs
+in the library's CUDA kernels; there is no other implementation to fall back
+to, and a missing library raises instead of degrading."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+EXATTN_OK = 0
+STATUS_NAMES = {
+    0: "EXATTN_OK", 1: "EXATTN_ERR_NULL", 2: "EXATTN_ERR_SHAPE", 3: "EXATTN_ERR_ALIGN",
+    4: "EXATTN_ERR_UNSUPPORTED", 5: "EXATTN_ERR_ARCH", 6: "EXATTN_ERR_WORKSPACE",
+    7: "EXATTN_ERR_CUDA", 8: "EXATTN_ERR_TIMEOUT", 9: "EXATTN_ERR_VALUE",
+}
+# Every entry point include/exattn.h declares.
+EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "exattn_status_string",
+           "exattn_device_error", "exattn_version")
+
+
+class ExattnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libexattn.so; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise ImportError(
+                    f"{path} is missing: build it with `python -m exact_attention_67_gb300.build` "
+                    "(the CUDA library is the only implementation)")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+        lib.attn_bwd.restype = i
+        lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+        lib.attn_bwd_workspace_size.restype = sz
+        lib.exattn_status_string.argtypes = [i]
+        lib.exattn_status_string.restype = ctypes.c_char_p
+        lib.exattn_device_error.argtypes = []
+        lib.exattn_device_error.restype = i
+        lib.exattn_version.argtypes = []
+        lib.exattn_version.restype = i
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().exattn_status_string(int(status)).decode()
+
+
+def _check(status: int):
+    if status != EXATTN_OK:
+        raise ExattnError(status, status_string(status))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _shape4(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, N, d], got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return tuple(t.shape)
+
+
+def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """C ``attn_fwd`` on torch tensors: q, k, v, o bf16 [B, H, N, d]; lse fp32
+    [B, H, N].  Asynchronous on ``stream`` (default: torch's current stream)."""
+    B, H, N, d = _shape4(q, "q")
+    for n, t in (("k", k), ("v", v), ("o", o)):
+        if _shape4(t, n) != (B, H, N, d):
+            raise ValueError(f"{n} shape {tuple(t.shape)} != q shape {(B, H, N, d)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                           float(scale), _stream(stream)))
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    return int(load().attn_bwd_workspace_size(B, H, N, d, int(bool(causal))))
+
+
+def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """C ``attn_bwd`` on torch tensors.  ``workspace`` is a CUDA tensor of at
+    least ``attn_bwd_workspace_size`` bytes."""
+    B, H, N, d = _shape4(q, "q")
+    for n, t in (("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if _shape4(t, n) != (B, H, N, d):
+            raise ValueError(f"{n} shape {tuple(t.shape)} != q shape {(B, H, N, d)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                           _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), ws_bytes,
+                           _stream(stream)))
+
+
+def device_error() -> int:
+    """Synchronise and read/clear the kernels' watchdog word (0 = clean)."""
+    return int(load().exattn_device_error())
+
+
+def version() -> int:
+    return int(load().exattn_version())

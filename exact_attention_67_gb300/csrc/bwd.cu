@@ -1,0 +1,599 @@
+// bwd.cu -- attention backward for sm_103a, recomputing S and P tile by tile
+// from the stored logsumexp ("Gemini 3 Flash的注意力内核重写：算子融合如何实现
+// 亚毫秒级推理", §4 重计算: keep only the row statistics, recompute the QK^T
+// blocks in the backward pass and stream the gradients).  With
+// P_ij = exp(scale q_i.k_j - lse_i), dP_ij = dO_i.v_j, D_i = dO_i.O_i and
+// dS_ij = P_ij (dP_ij - D_i) (the softmax vector-Jacobian product):
+//     dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
+//
+// Three kernels, no atomics (every output element is summed by one CTA in a
+// fixed order, so results are bit-identical run to run):
+//   1. bwd_rowdot_kernel: D_i = sum_c dO_ic O_ic (bandwidth bound).
+//   2. bwd_dkdv_kernel: one CTA per 128-key tile; streams 64-query tiles of
+//      Q and dO (TMA ring); per tile the tensor core computes S^T = K Q_i^T
+//      and dP^T = V dO_i^T into TMEM, a warpgroup (thread = key row) turns them
+//      into P^T and dS^T (bf16, written back over S^T and dP^T), and the
+//      tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
+//      S^T/dP^T are double buffered so the next tile's products overlap the
+//      current elementwise work.
+//   3. bwd_dq_kernel: one CTA per 128-query tile; streams 64-key tiles of K and
+//      V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (bf16) written back, and
+//      dQ += dS K_j accumulated in TMEM.
+// Causal: key tiles wholly above the diagonal are skipped, diagonal tiles are
+// masked element by element (key j visible to query i iff j <= i).
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace exattn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- D_i
+template <int D>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         float* __restrict__ Dout, long long rows) {
+  constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
+  constexpr int RPW = 32 / TPR;
+  const int lane = threadIdx.x & 31;
+  const long long warp_g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int sub = lane / TPR, part = lane % TPR;
+  for (long long r0 = warp_g * RPW; r0 < rows; r0 += n_warps * RPW) {
+    const long long r = r0 + sub;
+    float acc = 0.f;
+    if (r < rows) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + r * D) + part);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + r * D) + part);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(a2[e]);
+        const float2 fb = __bfloat1622float2(b2[e]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (r < rows && part == 0) Dout[r] = acc;
+  }
+}
+
+// ---------------------------------------------------------------- dK, dV
+template <int D>
+struct DkdvCfg {
+  static constexpr int BM = 128;  // keys per CTA (TMEM lanes)
+  static constexpr int BR = 64;   // queries per step
+  static constexpr int NCHUNK = D / 64;
+  static constexpr int KCHUNK = BM * 128;  // bytes of one 64-column chunk of a 128-row tile
+  static constexpr int QCHUNK = BR * 128;  // ... of a 64-row tile
+  static constexpr int KTILE = NCHUNK * KCHUNK;
+  static constexpr int QTILE = NCHUNK * QCHUNK;
+  static constexpr int STAGES = (D == 64) ? 4 : 3;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KTILE;
+  static constexpr int OFF_Q = OFF_V + KTILE;
+  static constexpr int OFF_DO = OFF_Q + STAGES * QTILE;
+  static constexpr int OFF_STAT = OFF_DO + STAGES * QTILE;  // per stage: lse2[BR], D[BR]
+  static constexpr int OFF_BAR = OFF_STAT + STAGES * 2 * BR * 4;
+  // At least 120 KB so that only one CTA (which holds all 512 TMEM columns) fits on an SM.
+  static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
+  static constexpr int THREADS = 192;  // warps 0-3 elementwise, 4 producer, 5 MMA
+  static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_BUF = 256, TM_COLS = 512;  // buffer b: S^T at +128b, dP^T at +128b+64
+};
+
+template <int STAGES>
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t st_full[STAGES], st_empty[STAGES];  // streamed operands of one step
+  uint64_t s_full[2];                          // both products of buffer b ready
+  uint64_t p_full[2];                          // elementwise results of buffer b written
+  uint64_t acc_done;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const float* __restrict__ lse, const float* __restrict__ Dws, __nv_bfloat16* __restrict__ dk,
+                    __nv_bfloat16* __restrict__ dv, int N, int BH, int n_ktiles, float scale, float scale_log2,
+                    unsigned* err) {
+  using C = DkdvCfg<D>;
+  using Bars = BwdBars<C::STAGES>;
+  static_assert(sizeof(Bars) <= 512, "barrier block too large");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Under the causal mask the first key tiles meet the most queries: run them first.
+  const int kt = static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int k0 = kt * C::BM;
+  const int nq_total = (N + C::BR - 1) / C::BR;
+  const int i_begin = CAUSAL ? (k0 / C::BR) : 0;
+  const int nq = nq_total - i_begin;  // >= 1 since k0 < N
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars->st_full[s], 1);
+      mbar_init(&bars->st_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 128);
+    }
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, err};
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_keep = l2_policy_evict_last();  // Q, dO are re-read by every key tile of the head
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KTILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, k0, bh, pol_keep);
+        tma_load_3d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, k0, bh, pol_keep);
+      }
+    }
+    int issued = 0;
+    for (int it = 0; it < nq; ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t ph = (it / C::STAGES) & 1;
+      if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
+      const int qi0 = (i_begin + it) * C::BR;
+      float* st_lse2 = stat + s * 2 * C::BR;
+      float* st_D = st_lse2 + C::BR;
+      for (int e = lane; e < C::BR; e += 32) {
+        const int qi = qi0 + e;
+        const bool valid = qi < N;
+        // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
+        st_lse2[e] = valid ? lse[static_cast<size_t>(bh) * N + qi] * kLog2e : INFINITY;
+        st_D[e] = valid ? Dws[static_cast<size_t>(bh) * N + qi] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QTILE);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(&tm_q, &bars->st_full[s], smem + C::OFF_Q + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, bh,
+                      pol_keep);
+          tma_load_3d(&tm_do, &bars->st_full[s], smem + C::OFF_DO + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, bh,
+                      pol_keep);
+        }
+      }
+      issued = it + 1;
+    }
+    if (lane == 0 && *reinterpret_cast<volatile int*>(&bars->abort)) {
+      mbar_wait_drain(&bars->kv_full, 0, err);
+      for (int it = max(0, issued - C::STAGES); it < issued; ++it)
+        mbar_wait_drain(&bars->st_full[it % C::STAGES], (it / C::STAGES) & 1, err);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, C::BR, 0, 0);  // K (or V) x Q^T (or dO^T): both K-major
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);    // TMEM operand x (Q or dO), MN-major
+      const uint32_t k_base = smem_u32(smem + C::OFF_K);
+      const uint32_t v_base = smem_u32(smem + C::OFF_V);
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      const uint32_t do_base = smem_u32(smem + C::OFF_DO);
+      auto issue_products = [&](int it) {
+        const int s = it % C::STAGES, b = it & 1;
+        const uint32_t qa = q_base + s * C::QTILE, da = do_base + s * C::QTILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
+          mma_ss(tmem + C::TM_BUF + b * 128, sdesc_sw128(k_base + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024),
+                 idesc_s, kk > 0);
+          mma_ss(tmem + C::TM_BUF + b * 128 + 64, sdesc_sw128(v_base + ko, 16, 1024),
+                 sdesc_sw128(da + qo, 16, 1024), idesc_s, kk > 0);
+        }
+      };
+      bool ok = mbar_wait(&bars->kv_full, 0, wc);
+      if (ok) ok = mbar_wait(&bars->st_full[0], 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_products(0);
+        mma_commit(&bars->s_full[0]);
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        const int s = it % C::STAGES, b = it & 1;
+        if (it + 1 < nq) {
+          const int s1 = (it + 1) % C::STAGES;
+          if (!(ok = mbar_wait(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1, wc))) break;
+          tc_fence_after();
+          issue_products(it + 1);
+          mma_commit(&bars->s_full[b ^ 1]);
+        }
+        if (!(ok = mbar_wait(&bars->p_full[b], (it >> 1) & 1, wc))) break;
+        tc_fence_after();
+        const uint32_t qa = q_base + s * C::QTILE, da = do_base + s * C::QTILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BR / 16; ++kk) {
+          // dV += P^T dO_i ; dK += dS^T Q_i  (operands over the first 32 columns of S^T / dP^T)
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_BUF + b * 128 + kk * 8,
+                 sdesc_sw128(da + kk * 16 * 128, C::QCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + kk * 8,
+                 sdesc_sw128(qa + kk * 16 * 128, C::QCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars->st_empty[s]);
+      }
+      if (ok) mma_commit(&bars->acc_done);
+      mma_commit(&bars->mma_done);
+      mbar_wait_drain(&bars->mma_done, 0, err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise (thread = key row)
+    const int row = warp * 32 + lane;
+    const int key = k0 + row;
+    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    for (int it = 0; ok && it < nq; ++it) {
+      const int s = it % C::STAGES, b = it & 1;
+      if (!(ok = mbar_wait(&bars->s_full[b], (it >> 1) & 1, wc))) break;
+      // The row statistics of this step were written by the producer's threads.
+      if (!(ok = mbar_wait(&bars->st_full[s], (it / C::STAGES) & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(tb, sr[0]);
+      tmem_ld32(tb + 32, sr[1]);
+      tmem_ld32(tb + 64, dr[0]);
+      tmem_ld32(tb + 96, dr[1]);
+      tmem_wait_ld();
+      const float* st_lse2 = stat + s * 2 * C::BR;
+      const float* st_D = st_lse2 + C::BR;
+      const int qi0 = (i_begin + it) * C::BR;
+      const bool need_mask = CAUSAL && (qi0 < k0 + C::BM);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[16], dk_[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = h * 32 + 2 * e + u;
+            float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, -st_lse2[c]));
+            if (need_mask && qi0 + c < key) p = 0.f;
+            pv[u] = p;
+            dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - st_D[c]);
+          }
+          pk[e] = pack_bf16x2(pv[0], pv[1]);
+          dk_[e] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(tb + h * 16, pk);         // P^T over S^T
+        tmem_st16(tb + 64 + h * 16, dk_);   // dS^T over dP^T
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[b]);
+    }
+    if (ok) ok = mbar_wait(&bars->acc_done, 0, wc);
+    if (ok) {
+      tc_fence_after();
+      const size_t base = (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tacc = tmem + lane_bits + (which == 0 ? C::TM_DK : C::TM_DV);
+        const float mul = which == 0 ? scale : 1.f;
+        __nv_bfloat16* dst_row = (which == 0 ? dk : dv) + base;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tacc + c * 32, r);
+          tmem_wait_ld();
+          if (key < N) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D>
+struct DqCfg {
+  static constexpr int BM = 128;  // queries per CTA (TMEM lanes)
+  static constexpr int BN = 64;   // keys per step
+  static constexpr int NCHUNK = D / 64;
+  static constexpr int QCHUNK = BM * 128;
+  static constexpr int KCHUNK = BN * 128;
+  static constexpr int QTILE = NCHUNK * QCHUNK;
+  static constexpr int KTILE = NCHUNK * KCHUNK;
+  static constexpr int STAGES = (D == 64) ? 4 : 3;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + QTILE;
+  static constexpr int OFF_K = OFF_DO + QTILE;
+  static constexpr int OFF_V = OFF_K + STAGES * KTILE;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
+  // At least 120 KB so that only one CTA (which holds all 512 TMEM columns) fits on an SM.
+  static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TM_DQ = 0, TM_BUF = 128, TM_COLS = 512;  // buffer b: S at +128b, dP at +128b+64
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const float* __restrict__ lse, const float* __restrict__ Dws, __nv_bfloat16* __restrict__ dq,
+                  int N, int BH, int n_qtiles, float scale, float scale_log2, unsigned* err) {
+  using C = DqCfg<D>;
+  using Bars = BwdBars<C::STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Under the causal mask the last query tiles meet the most keys: run them first.
+  const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int q0 = qt * C::BM;
+  const int nk_total = (N + C::BN - 1) / C::BN;
+  const int nk = CAUSAL ? min(nk_total, (q0 + C::BM - 1) / C::BN + 1) : nk_total;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);  // here: Q and dO tiles
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars->st_full[s], 1);
+      mbar_init(&bars->st_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 128);
+    }
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, err};
+
+  if (warp == 4) {
+    if (lane == 0) {
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_once = l2_policy_evict_first();
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::QTILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d(&tm_q, &bars->kv_full, smem + C::OFF_Q + c * C::QCHUNK, c * 64, q0, bh, pol_once);
+        tma_load_3d(&tm_do, &bars->kv_full, smem + C::OFF_DO + c * C::QCHUNK, c * 64, q0, bh, pol_once);
+      }
+      int issued = 0;
+      for (int it = 0; it < nk; ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (it / C::STAGES) & 1;
+        if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
+                      it * C::BN, bh, pol_keep);
+          tma_load_3d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
+                      it * C::BN, bh, pol_keep);
+        }
+        issued = it + 1;
+      }
+      if (*reinterpret_cast<volatile int*>(&bars->abort)) {
+        mbar_wait_drain(&bars->kv_full, 0, err);
+        for (int it = max(0, issued - C::STAGES); it < issued; ++it)
+          mbar_wait_drain(&bars->st_full[it % C::STAGES], (it / C::STAGES) & 1, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      const uint32_t do_base = smem_u32(smem + C::OFF_DO);
+      const uint32_t k_base = smem_u32(smem + C::OFF_K);
+      const uint32_t v_base = smem_u32(smem + C::OFF_V);
+      auto issue_products = [&](int it) {
+        const int s = it % C::STAGES, b = it & 1;
+        const uint32_t ka = k_base + s * C::KTILE, va = v_base + s * C::KTILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
+          mma_ss(tmem + C::TM_BUF + b * 128, sdesc_sw128(q_base + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024),
+                 idesc_s, kk > 0);
+          mma_ss(tmem + C::TM_BUF + b * 128 + 64, sdesc_sw128(do_base + qo, 16, 1024),
+                 sdesc_sw128(va + ko, 16, 1024), idesc_s, kk > 0);
+        }
+      };
+      bool ok = mbar_wait(&bars->kv_full, 0, wc);
+      if (ok) ok = mbar_wait(&bars->st_full[0], 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_products(0);
+        mma_commit(&bars->s_full[0]);
+      }
+      for (int it = 0; ok && it < nk; ++it) {
+        const int s = it % C::STAGES, b = it & 1;
+        if (it + 1 < nk) {
+          const int s1 = (it + 1) % C::STAGES;
+          if (!(ok = mbar_wait(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1, wc))) break;
+          tc_fence_after();
+          issue_products(it + 1);
+          mma_commit(&bars->s_full[b ^ 1]);
+        }
+        if (!(ok = mbar_wait(&bars->p_full[b], (it >> 1) & 1, wc))) break;
+        tc_fence_after();
+        const uint32_t ka = k_base + s * C::KTILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(tmem + C::TM_DQ, tmem + C::TM_BUF + b * 128 + kk * 8,
+                 sdesc_sw128(ka + kk * 16 * 128, C::KCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->st_empty[s]);
+      }
+      if (ok) mma_commit(&bars->acc_done);
+      mma_commit(&bars->mma_done);
+      mbar_wait_drain(&bars->mma_done, 0, err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise (thread = query row)
+    const int row = warp * 32 + lane;
+    const int qrow = q0 + row;
+    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    const bool valid = qrow < N;
+    const float lse2 = valid ? lse[static_cast<size_t>(bh) * N + qrow] * kLog2e : INFINITY;
+    const float Drow = valid ? Dws[static_cast<size_t>(bh) * N + qrow] : 0.f;
+    const float neg_lse2 = -lse2;
+    bool ok = true;
+    for (int it = 0; ok && it < nk; ++it) {
+      const int b = it & 1;
+      if (!(ok = mbar_wait(&bars->s_full[b], (it >> 1) & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(tb, sr[0]);
+      tmem_ld32(tb + 32, sr[1]);
+      tmem_ld32(tb + 64, dr[0]);
+      tmem_ld32(tb + 96, dr[1]);
+      tmem_wait_ld();
+      const int kj0 = it * C::BN;
+      const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > q0) || (kj0 + C::BN > N);
+      int lim = N - kj0;
+      if (CAUSAL) lim = min(lim, qrow - kj0 + 1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = h * 32 + 2 * e + u;
+            float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, neg_lse2));
+            if (need_mask && c >= lim) p = 0.f;
+            dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - Drow);
+          }
+          pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(tb + h * 16, pk);  // dS over S
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[b]);
+    }
+    if (ok) ok = mbar_wait(&bars->acc_done, 0, wc);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dst_row = dq + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_bits + C::TM_DQ + c * 32, r);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// ---------------------------------------------------------------- launch
+template <int D, bool CAUSAL>
+static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+  cudaError_t e;
+  {
+    const long long rows = static_cast<long long>(a.BH) * a.N;
+    const int rpb = 256 / (D / 8);  // rows per 256-thread block
+    long long blocks = (rows + rpb - 1) / rpb;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    bwd_rowdot_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.D, rows);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    using C = DkdvCfg<D>;
+    auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+    if ((e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device)) != cudaSuccess)
+      return e;
+    const int n_kt = (a.N + C::BM - 1) / C::BM;
+    kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
+        *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
+        static_cast<__nv_bfloat16*>(a.dv), a.N, a.BH, n_kt, a.scale, a.scale_log2, a.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    using C = DqCfg<D>;
+    auto kern = bwd_dq_kernel<D, CAUSAL>;
+    if ((e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device)) != cudaSuccess)
+      return e;
+    const int n_qt = (a.N + C::BM - 1) / C::BM;
+    kern<<<static_cast<unsigned>(static_cast<long long>(n_qt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
+        *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.N, a.BH, n_qt,
+        a.scale, a.scale_log2, a.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
+  return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+}
+
+}  // namespace exattn

@@ -1,0 +1,377 @@
+// fwd.cu -- fused attention forward for sm_103a.
+//
+// One kernel computes O = softmax(scale Q K^T [+ causal mask]) V and the
+// per-row logsumexp, keeping S and P on chip ("Gemini 3 Flash的注意力内核重写：
+// 算子融合如何实现亚毫秒级推理", §1 内核融合策略: load Q/K/V blocks, do QK^T,
+// softmax and PV on chip, write only O).  Keys are visited in tiles with a
+// running max and running sum (same page, §3 在线softmax算法); tiles of keys
+// wholly above the causal diagonal are never visited ("提示词再优也救不了的性能
+// 黑洞…", 第一章, causal=True skips the upper triangle).
+//
+// GB300 mapping (one CTA per SM, 320 threads):
+//   * the CTA owns two 128-row query tiles (256 rows) of one (batch, head);
+//     they share one stream of 128-row K/V tiles;
+//   * warp 8 issues TMA loads: both Q tiles once, then K_j and V_j into
+//     STAGES-deep rings of 128-byte-swizzled shared-memory tiles;
+//   * warp 9 (one thread) issues tcgen05 MMAs: S_t = Q_t K_j^T into TMEM
+//     (fp32, 128 lanes x 128 columns per tile) and O_t += P_t V_j with P_t
+//     read straight from TMEM;
+//   * warps 0-3 and 4-7 are the softmax warpgroups of tile 0 and tile 1; a
+//     thread owns one query row (= one TMEM lane).  Per key tile it reads its
+//     128 scores, updates the running max, rescales the running sum and the
+//     TMEM O row when the max has grown by more than 2^8 (the reference max
+//     is otherwise kept; the final normalisation by the same reference makes
+//     the result identical), writes P = 2^(s*scale*log2e - m) as bf16 over
+//     the S columns, and hands the tile back to the MMA warp.  While one
+//     warpgroup does its softmax the tensor core works on the other tile.
+//   * epilogue: O_t / l rounded to bf16 and lse = (m + log2 l) ln 2.
+// TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace exattn {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                   // query rows per tile (TMEM lanes)
+  static constexpr int BN = 128;                   // keys per K/V tile
+  static constexpr int NCHUNK = D / 64;            // 128-byte swizzle atoms across d
+  static constexpr int CHUNK_BYTES = 128 * 128;    // 128 rows x 128 bytes
+  static constexpr int TILE_BYTES = NCHUNK * CHUNK_BYTES;
+  static constexpr int STAGES = (D == 64) ? 4 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + barriers + alignment slack
+  static_assert(SMEM_BYTES > 120 * 1024, "one CTA per SM: it holds all 512 TMEM columns");
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TM_S = 0, TM_O = 256, TM_COLS = 512;
+};
+
+template <int STAGES>
+struct FwdBars {
+  uint64_t q_full[2];
+  uint64_t k_full[STAGES], k_empty[STAGES];
+  uint64_t v_full[STAGES], v_empty[STAGES];
+  uint64_t s_full[2];  // S_t ready (also: every earlier MMA of the CTA done)
+  uint64_t p_full[2];  // P_t written to TMEM by the 128 softmax threads
+  uint64_t o_full[2];  // last P_t V_j of tile t done
+  uint64_t mma_done;   // every MMA of the CTA done (teardown)
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Rescale threshold for the running max, in log2 units: P stays below 2^8.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse_out, int N, int BH, int n_pairs, float scale_log2, unsigned* err) {
+  using C = FwdCfg<D>;
+  using Bars = FwdBars<C::STAGES>;
+  static_assert(sizeof(Bars) <= 512, "barrier block too large");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Heaviest work first: under the causal mask the last query pairs see the most keys.
+  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int q0 = pair * 2 * C::BM;
+  const int nkv_total = (N + C::BN - 1) / C::BN;
+  // Key tiles visited by query tile t (0 if the tile lies wholly past N).
+  auto tiles_for = [&](int t) {
+    const int r0 = q0 + t * C::BM;
+    return (r0 >= N) ? 0 : (CAUSAL ? min(nkv_total, r0 / C::BN + 1) : nkv_total);
+  };
+  const int nkv0 = tiles_for(0), nkv1 = tiles_for(1);
+  const int n_iter = max(nkv0, nkv1);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_full[t], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, err};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query pair of the head
+      const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? nkv0 : nkv1) == 0) continue;
+        mbar_arrive_expect_tx(&bars->q_full[t], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(&tm_q, &bars->q_full[t], smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
+                      q0 + t * C::BM, bh, pol_q);
+      }
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < n_iter; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(&tm_k, &bars->k_full[s], smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
+                      j * C::BN, bh, pol_kv);
+        issued_k = j + 1;
+        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(&tm_v, &bars->v_full[s], smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
+                      j * C::BN, bh, pol_kv);
+        issued_v = j + 1;
+      }
+      if (*reinterpret_cast<volatile int*>(&bars->abort)) {
+        // Never leave a copy in flight into shared memory this CTA is about to release.
+        for (int t = 0; t < 2; ++t)
+          if ((t == 0 ? nkv0 : nkv1) > 0) mbar_wait_drain(&bars->q_full[t], 0, err);
+        for (int j = max(0, issued_k - C::STAGES); j < issued_k; ++j)
+          mbar_wait_drain(&bars->k_full[j % C::STAGES], (j / C::STAGES) & 1, err);
+        for (int j = max(0, issued_v - C::STAGES); j < issued_v; ++j)
+          mbar_wait_drain(&bars->v_full[j % C::STAGES], (j / C::STAGES) & 1, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);  // Q, K both K-major
+      constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);      // P from TMEM, V MN-major
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      const uint32_t k_base = smem_u32(smem + C::OFF_K);
+      const uint32_t v_base = smem_u32(smem + C::OFF_V);
+
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t qa = q_base + t * C::TILE_BYTES;
+        const uint32_t ka = k_base + stage * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + C::TM_S + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int stage, bool acc) {
+        const uint32_t va = v_base + stage * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          mma_ts(tmem + C::TM_O + t * 128, tmem + C::TM_S + t * 128 + kk * 8,
+                 sdesc_sw128(va + kk * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if ((t == 0 ? nkv0 : nkv1) > 0) ok = mbar_wait(&bars->q_full[t], 0, wc);
+      if (ok && n_iter > 0) ok = mbar_wait(&bars->k_full[0], 0, wc);
+      if (ok && n_iter > 0) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if ((t == 0 ? nkv0 : nkv1) == 0) continue;
+          issue_s(t, 0);
+          mma_commit(&bars->s_full[t]);
+        }
+        mma_commit(&bars->k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_iter; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        const int s1 = (j + 1) % C::STAGES;
+        const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+        bool v_ready = false, k_ready = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || j >= (t == 0 ? nkv0 : nkv1)) continue;
+          if (!(ok = mbar_wait(&bars->p_full[t], j & 1, wc))) continue;
+          if (!v_ready) {
+            if (!(ok = mbar_wait(&bars->v_full[s], ph, wc))) continue;
+            v_ready = true;
+          }
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          if (j + 1 < (t == 0 ? nkv0 : nkv1)) {
+            if (!k_ready) {
+              if (!(ok = mbar_wait(&bars->k_full[s1], ph1, wc))) continue;
+              k_ready = true;
+              tc_fence_after();
+            }
+            issue_s(t, s1);
+            mma_commit(&bars->s_full[t]);
+          } else {
+            mma_commit(&bars->o_full[t]);
+          }
+        }
+        if (v_ready) mma_commit(&bars->v_empty[s]);
+        if (k_ready) mma_commit(&bars->k_empty[s1]);
+      }
+      // Nothing may still read shared memory or write TMEM once the CTA tears down.
+      mma_commit(&bars->mma_done);
+      mbar_wait_drain(&bars->mma_done, 0, err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;          // query row within the tile == TMEM lane
+    const int row_g = q0 + t * C::BM + row;  // query row within the head
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + C::TM_S + t * 128;
+    const uint32_t tO = tmem + lane_bits + C::TM_O + t * 128;
+    float m_ref = -INFINITY;  // reference max, log2 units of the scaled logits
+    float l = 0.f;            // running sum of 2^(x - m_ref)
+    bool ok = (t == 0 ? nkv0 : nkv1) > 0;
+    for (int j = 0; ok && j < (t == 0 ? nkv0 : nkv1); ++j) {
+      if (!(ok = mbar_wait(&bars->s_full[t], j & 1, wc))) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+      tmem_wait_ld();
+
+      const int kv0 = j * C::BN;
+      const bool need_mask = (CAUSAL && j == (t == 0 ? nkv0 : nkv1) - 1) || (kv0 + C::BN > N);
+      float mx = -INFINITY;
+      if (need_mask) {
+        int lim = N - kv0;
+        if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+      }
+      const float m_new = fmaxf(m_ref, mx * scale_log2);
+      // Move the reference max only when it grew by more than the threshold.
+      float alpha = 1.f;
+      bool rescale_warp = false;
+      if (j == 0) {
+        m_ref = m_new;
+      } else {
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        rescale_warp = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2(m_ref - m_new);
+          m_ref = m_new;
+        }
+      }
+      const float neg_m = -m_ref;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), scale_log2, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), scale_log2, neg_m));
+          rs0 += p0;
+          rs1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);  // P_t over the first 64 columns of S_t
+      }
+      l = l * alpha + (rs0 + rs1);
+      if (rescale_warp) {
+        // S_t(j) ready implies P_t(j-1) V_{j-1} has completed: the O row is stable.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o_r[32];
+          tmem_ld32(tO + c * 32, o_r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o_r[e] = __float_as_uint(__uint_as_float(o_r[e]) * alpha);
+          tmem_st32(tO + c * 32, o_r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && (t == 0 ? nkv0 : nkv1) > 0) ok = mbar_wait(&bars->o_full[t], 0, wc);
+    if (ok && (t == 0 ? nkv0 : nkv1) > 0) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * N + row_g) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o_r[32];
+        tmem_ld32(tO + c * 32, o_r);
+        tmem_wait_ld();
+        if (row_g < N) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o_r[2 * e]) * inv_l, __uint_as_float(o_r[2 * e + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (row_g < N) lse_out[static_cast<size_t>(bh) * N + row_g] = (m_ref + log2f(l)) * 0.6931471805599453f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
+  if (e != cudaSuccess) return e;
+  const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  const long long grid = static_cast<long long>(n_pairs) * a.BH;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
+      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.N, a.BH, n_pairs, a.scale_log2, a.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+}
+
+}  // namespace exattn

@@ -1,0 +1,126 @@
+/*
+ * exattn.h -- C ABI of the fused exact-attention library for NVIDIA GB300
+ * (sm_103a), libexattn.so.
+ *
+ * The operation is exact scaled-dot-product attention,
+ *
+ *     O = softmax(scale * Q K^T  [+ causal mask]) V,
+ *
+ * computed as one fused, tiled kernel with an online softmax so that the
+ * score matrix S and the probability matrix P never reach device memory
+ * ("Gemini 3 Flash的注意力内核重写：算子融合如何实现亚毫秒级推理",
+ * §1 内核融合策略, §2 分块, §3 在线softmax算法), and its gradient, which
+ * recomputes S and P tile by tile from the stored per-row statistic (same
+ * page, §4 重计算).  The causal flag follows the flash_attn_func example of
+ * "提示词再优也救不了的性能黑洞：Transformer注意力计算冗余分析（含
+ * FlashAttention-3内核级优化验证数据）", 第一章: key j is visible to query i
+ * iff j <= i (square, top-left aligned); key tiles wholly above the diagonal
+ * are skipped.
+ *
+ * Conventions shared by every call
+ *   - Q, K, V, O, dO, dQ, dK, dV are bf16 (2-byte __nv_bfloat16), device
+ *     pointers, contiguous [B, H, N, d] with d fastest (the [B, H, T, D]
+ *     layout of the "提示词再优…" page, §2.3), 16-byte aligned.
+ *   - lse is fp32 [B, H, N], 4-byte aligned: lse[b,h,i] = m_i + ln(l_i), the
+ *     natural-log logsumexp of row i of the scaled, masked logits (the row
+ *     max m_i and normaliser l_i of the "Gemini 3 Flash…" page, §4, folded
+ *     into one number).
+ *   - 1 <= B, 1 <= H, 1 <= N, B*H*N < 2^31, d in {64, 128}; scale finite, > 0.
+ *     N need not be a multiple of the tile size.
+ *   - All pointers belong to the caller, who allocates and frees them; the
+ *     library allocates no device memory and never synchronises.  Inputs are
+ *     read only; outputs must not alias inputs or each other.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) on the current device.  The return value reports
+ *     argument errors and launch errors; faults during execution surface at
+ *     the caller's next synchronisation, and the kernels' own watchdog
+ *     (every internal wait is bounded) is read with exattn_device_error().
+ *   - Only sm_103 devices are supported (EXATTN_ERR_ARCH otherwise).
+ */
+#ifndef EXATTN_H
+#define EXATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EXATTN_OK = 0,
+  EXATTN_ERR_NULL = 1,        /* a required pointer is NULL */
+  EXATTN_ERR_SHAPE = 2,       /* B, H or N out of range */
+  EXATTN_ERR_ALIGN = 3,       /* a pointer is not aligned as stated above */
+  EXATTN_ERR_UNSUPPORTED = 4, /* d not in {64, 128} */
+  EXATTN_ERR_ARCH = 5,        /* current device is not sm_103 */
+  EXATTN_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required */
+  EXATTN_ERR_CUDA = 7,        /* a CUDA runtime/driver call or a launch failed */
+  EXATTN_ERR_TIMEOUT = 8,     /* a kernel's bounded internal wait gave up */
+  EXATTN_ERR_VALUE = 9        /* scale not finite or not positive */
+} exattn_status;
+
+/*
+ * attn_fwd -- forward pass.
+ *   q, k, v : inputs, bf16 [B, H, N, d].
+ *   o       : output, bf16 [B, H, N, d]; O_i = sum_j P_ij V_j, rounded to
+ *             nearest-even bf16 from fp32.
+ *   lse     : output, fp32 [B, H, N] (see above); it is the exact input that
+ *             attn_bwd expects.
+ *   causal  : 0 = full attention, nonzero = causal mask (j <= i).
+ *   scale   : multiplies Q K^T before masking and softmax (1/sqrt(d) usual).
+ *   stream  : cudaStream_t.
+ * Arithmetic: bf16 products accumulated in fp32 on the tensor cores; the
+ * softmax runs in fp32; P is rounded to bf16 before the P V product.
+ * Returns an exattn_status.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             int causal, float scale, void* stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs for
+ * this shape (fp32 row terms D_i = sum_c dO_ic O_ic, one per query row).
+ * Returns 0 for an invalid shape.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d, int causal);
+
+/*
+ * attn_bwd -- backward pass of attn_fwd for output gradient dO.
+ *   q, k, v, o, lse : the forward's inputs and outputs (o and lse exactly as
+ *                     attn_fwd wrote them).
+ *   dO              : bf16 [B, H, N, d], gradient of the loss w.r.t. O.
+ *   dq, dk, dv      : outputs, bf16 [B, H, N, d].
+ *   workspace       : device memory of at least
+ *                     attn_bwd_workspace_size(B, H, N, d, causal) bytes,
+ *                     16-byte aligned, owned by the caller; its contents on
+ *                     entry are ignored and on return are unspecified.
+ * It computes D_i = sum_c dO_ic O_ic, then for every tile pair recomputes
+ * P_ij = exp(scale q_i.k_j - lse_i), dP_ij = dO_i.v_j, dS_ij = P_ij (dP_ij - D_i)
+ * and accumulates dV_j += P_ij dO_i, dK_j += scale dS_ij q_i (one pass over
+ * query tiles per key tile) and dQ_i += scale dS_ij k_j (one pass over key
+ * tiles per query tile).  No atomics: every output element is summed by one
+ * CTA in a fixed order, so results are bit-identical from run to run.
+ * Returns an exattn_status.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/* Human-readable text of an exattn_status (static storage, never NULL). */
+const char* exattn_status_string(int status);
+
+/*
+ * exattn_device_error -- synchronises the current device, reads and clears
+ * the kernels' watchdog word.  Returns EXATTN_OK if no bounded wait gave up
+ * since the last call, EXATTN_ERR_TIMEOUT if one did (the outputs of the
+ * affected launches are then garbage), EXATTN_ERR_CUDA if the read failed.
+ */
+int exattn_device_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int exattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXATTN_H */

@@ -1,0 +1,108 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+on seeded inputs and compare with the fp64 oracle.
+
+Tolerances (fixed for this method; bf16 inputs, fp32 accumulation):
+  O    max |err| <= 1e-2 beyond bf16 output rounding, mean |err| <= 1e-3
+  lse  max |err| <= 1e-3
+  dQ, dK, dV  ||err||_F / ||ref||_F <= 2e-2
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+TOL_O_MAX = 1e-2
+TOL_O_MEAN = 1e-3
+TOL_LSE_MAX = 1e-3
+TOL_GRAD_REL = 2e-2
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy()
+
+
+def run_gpu(q, k, v, do, causal: bool, scale: float, bwd: bool = True):
+    """Copy the CPU bf16 inputs to the GPU, run attn_fwd (and attn_bwd)."""
+    import exact_attention_67_gb300 as ex
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = ex.forward(qd, kd, vd, causal, scale)
+    out = {"o": o, "lse": lse}
+    if bwd:
+        dod = do.to(dev)
+        dq, dk, dv = ex.backward(qd, kd, vd, o, lse, dod, causal, scale)
+        out.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert ex.device_error() == 0, "a kernel watchdog fired"
+    return {n: t.cpu() for n, t in out.items()}
+
+
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |x| (8 significant bits): the error
+    that rounding the exact value to a bf16 output alone can make."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(ax)) - 8.0)
+
+
+def check_fwd(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what=""):
+    """O is bf16, so an exact result rounded to bf16 is already off by up to
+    half a bf16 ulp (0.0156 for |O| in [4, 8)).  The max-abs bound applies to
+    the error beyond that rounding; the raw max-abs error is reported too."""
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
+    assert np.all(np.isfinite(lse_gpu)), f"{what}: non-finite lse"
+    err = np.abs(o_gpu - o_ref)
+    beyond = err - bf16_half_ulp(o_ref)
+    lerr = np.abs(lse_gpu - lse_ref)
+    n_raw = int(np.count_nonzero(err > TOL_O_MAX))
+    info = (f"{what}: O max {err.max():.3e} (beyond bf16 rounding {beyond.max():.3e}; "
+            f"{n_raw} elements > {TOL_O_MAX} raw) mean {err.mean():.3e}; lse max {lerr.max():.3e}; "
+            f"max|O| {np.abs(o_ref).max():.3f}")
+    assert beyond.max() <= TOL_O_MAX, info
+    assert err.mean() <= TOL_O_MEAN, info
+    assert lerr.max() <= TOL_LSE_MAX, info
+    return info
+
+
+def rel_fro(a: np.ndarray, ref: np.ndarray) -> float:
+    return float(np.linalg.norm((a - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-30))
+
+
+def check_grads(pairs, what=""):
+    """Relative Frobenius error <= 2e-2.  A gradient whose exact value is zero
+    (a single key: dQ = 0 and dK = 0 because each row of dS sums to zero) has
+    no relative error; there the absolute error must stay below 1e-3."""
+    msgs = []
+    for name, g, ref in pairs:
+        assert np.all(np.isfinite(g)), f"{what}: non-finite {name}"
+        ref_norm = np.linalg.norm(ref.ravel())
+        if ref_norm <= 1e-9 * np.sqrt(max(ref.size, 1)):
+            a = float(np.max(np.abs(g - ref))) if g.size else 0.0
+            msgs.append(f"{name} zero-ref abs {a:.3e}")
+            assert a <= 1e-3, f"{what}: {name} abs err {a:.3e} on a zero gradient"
+            continue
+        r = rel_fro(g, ref)
+        msgs.append(f"{name} {r:.3e}")
+        assert r <= TOL_GRAD_REL, f"{what}: {name} rel-Fro {r:.3e} > {TOL_GRAD_REL}"
+    return f"{what}: " + ", ".join(msgs)
+
+
+def full_parity(orc, q, k, v, do, causal: bool, scale: float, bwd: bool = True, what=""):
+    """Whole-tensor comparison (small shapes)."""
+    res = run_gpu(q, k, v, do, causal, scale, bwd)
+    qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
+    o_ref, lse_ref = orc.attention_fwd(qf, kf, vf, causal, scale)
+    msg = check_fwd(to_f64(res["o"]), res["lse"].double().numpy(), o_ref, lse_ref, what)
+    if bwd:
+        dq_ref, dk_ref, dv_ref = orc.attention_bwd(qf, kf, vf, to_f64(do), causal, scale)
+        msg += " | " + check_grads([("dQ", to_f64(res["dq"]), dq_ref), ("dK", to_f64(res["dk"]), dk_ref),
+                                    ("dV", to_f64(res["dv"]), dv_ref)], what)
+    return res, msg
+
+
+def sample_rows(N: int, n: int, seed: int) -> np.ndarray:
+    """Spread sample of row indices that always includes the first and last rows
+    and both sides of every 128-row tile boundary it touches."""
+    rng = np.random.default_rng(seed)
+    base = {0, 1, N - 1, N - 2, min(127, N - 1), min(128, N - 1)}
+    extra = rng.choice(N, size=min(n, N), replace=False)
+    return np.array(sorted(base | set(int(x) for x in extra)), dtype=np.int32)

@@ -1,0 +1,123 @@
+"""The C-ABI boundary on the host: the library loads, exports every entry point
+include/exattn.h declares, and rejects bad arguments before touching CUDA.
+
+No test here launches a kernel or needs a GPU: every call below fails
+validation, which happens before the first CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "exattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_67_gb300 import build as b
+    b.build()
+    from exact_attention_67_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\**\s+\**([a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    from exact_attention_67_gb300._lib import EXPORTS
+    assert sorted(EXPORTS) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    from exact_attention_67_gb300 import _lib
+    for code in range(0, 10):
+        s = _lib.status_string(code)
+        assert s and s != "unknown exattn status"
+    assert _lib.status_string(12345) == "unknown exattn status"
+    assert lib.exattn_version() >= 100
+
+
+# fake, never dereferenced, 256-byte aligned "device" addresses
+P = [0x100000 + 0x100000 * i for i in range(12)]
+
+
+def fwd(lib, q=P[0], k=P[1], v=P[2], o=P[3], lse=P[4], B=1, H=2, N=256, d=64, causal=0, scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+def bwd(lib, ptrs=None, B=1, H=2, N=256, d=64, causal=0, scale=0.125, ws=P[11], ws_bytes=1 << 20):
+    p = list(P[:9]) if ptrs is None else ptrs
+    return lib.attn_bwd(*p, B, H, N, d, causal, scale, ws, ws_bytes, None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, q=None) == 1
+    assert fwd(lib, lse=None) == 1
+    assert fwd(lib, B=0) == 2
+    assert fwd(lib, H=-1) == 2
+    assert fwd(lib, N=0) == 2
+    assert fwd(lib, B=1 << 16, H=1 << 10, N=1 << 10) == 2   # B*H*N >= 2^31
+    assert fwd(lib, d=96) == 4
+    assert fwd(lib, d=256) == 4
+    assert fwd(lib, scale=0.0) == 9
+    assert fwd(lib, scale=-1.0) == 9
+    assert fwd(lib, scale=float("inf")) == 9
+    assert fwd(lib, scale=float("nan")) == 9
+    assert fwd(lib, q=P[0] + 8) == 3
+    assert fwd(lib, o=P[3] + 2) == 3
+    assert fwd(lib, lse=P[4] + 2) == 3
+
+
+def test_bwd_validation(lib):
+    for i in range(9):
+        p = list(P[:9])
+        p[i] = None
+        assert bwd(lib, ptrs=p) == 1
+    assert bwd(lib, N=0) == 2
+    assert bwd(lib, d=32) == 4
+    assert bwd(lib, scale=float("nan")) == 9
+    for i in (0, 1, 2, 3, 4, 6, 7, 8):
+        p = list(P[:9])
+        p[i] += 4
+        assert bwd(lib, ptrs=p) == 3
+    assert bwd(lib, ws=None) == 6
+    assert bwd(lib, ws_bytes=16) == 6
+    assert bwd(lib, ws=P[11] + 4) == 3
+
+
+def test_workspace_size(lib):
+    assert lib.attn_bwd_workspace_size(1, 2, 256, 64, 0) == 2048
+    assert lib.attn_bwd_workspace_size(1, 16, 8192, 128, 1) == 16 * 8192 * 4
+    assert lib.attn_bwd_workspace_size(1, 1, 3, 64, 0) == 256
+    assert lib.attn_bwd_workspace_size(0, 1, 3, 64, 0) == 0
+    assert lib.attn_bwd_workspace_size(1, 1, 3, 80, 0) == 0
+
+
+def test_python_binding_rejects_bad_tensors():
+    import torch
+    from exact_attention_67_gb300 import _lib
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        _lib._shape4(q, "q")
+    with pytest.raises(ValueError):
+        _lib._shape4(torch.zeros(8, 64, dtype=torch.bfloat16), "q")
+    with pytest.raises(ValueError):  # CPU tensor: the library has no CPU path
+        _lib._shape4(torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16), "q")
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from exact_attention_67_gb300 import _lib
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "library_path", lambda: str(tmp_path / "nope.so"))
+    with pytest.raises(ImportError):
+        _lib.load()
