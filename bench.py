@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark: fused exact attention, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole path over one batch of synthetic input:
+attn_fwd (fused forward), then the three backward kernels (row dots D_i,
+dK/dV, dQ).  The default workload is B=1, H=16, N=8192, d=128, causal, bf16
+(the N=8192 causal forward is the case the forward target is stated on).
+Prints ONE JSON line (rank 0).
+
+Timing: inputs resident in HBM; L2 is flushed (a 256 MiB write) before every
+step, outside the timed events; each kernel is bracketed by CUDA events on
+the launching stream; the step time is the sum of its kernels' event times.
+TFLOPS use the algorithmic FLOP model 4*B*H*N^2*d (halved when causal) for
+the forward and 2.5x that for the backward.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (heads
+are independent: weak scaling, no data-path collective); the reported value
+is the FLOPs of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOPS (fwd, fwd+bwd) on 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOPS"
+FALLBACK_PEAK_TFLOPS = 1900.0   # profiling recipe fallback (bf16 burst) if no measured file
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=4, help="workload number 1-5 (default 4)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p.get("hbm_gbs", 0.0)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def kernel_source_sha(name: str) -> str:
+    src = {"attn_fwd_kernel": "fwd.cu", "bwd_dkdv_kernel": "bwd.cu", "bwd_dq_kernel": "bwd.cu",
+           "bwd_rowdot_kernel": "bwd.cu"}[name]
+    h = hashlib.sha256()
+    for f in (src, "ptx.cuh"):
+        with open(os.path.join(ROOT, "exact_attention_67_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(name: str, workload: str):
+    """Per-launch DRAM bytes of `name` from the committed ncu summary, if it was
+    taken on the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[workload][name]
+        if e.get("source_sha") != kernel_source_sha(name):
+            return None
+        return float(e["bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples with host timestamps."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, enabled: bool = True):
+        self.proc = None
+        self.path = None
+        self.idx = device_index
+        if not enabled:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                        ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                        rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+                    except (ValueError, IndexError):
+                        continue
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed region"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:3]
+            window = "nearest samples to a short timed region"
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+# ------------------------------------------------------------ CPU oracle legs
+def oracle_head_flops(w, n_rows: int) -> float:
+    """Algorithmic fwd+bwd FLOPs of an n_rows x n_rows leading block of one head."""
+    f = 4.0 * n_rows * n_rows * w.d
+    if w.causal:
+        f /= 2
+    return 3.5 * f
+
+
+def run_oracle_sample(w, q, k, v, do, head: int, n_rows: int):
+    """The oracle's full fwd + bwd on the leading n_rows x n_rows block of one
+    head (under the causal mask these rows see only these keys).  Returns
+    (seconds, threads)."""
+    import oracle
+    orc = oracle._load()
+    b, h = divmod(head, w.H)
+
+    def f64(t):
+        return t[b, h, :n_rows].float().double().numpy()
+
+    qf, kf, vf, dof = f64(q), f64(k), f64(v), f64(do)
+    nt = orc.default_threads()
+    t0 = time.perf_counter()
+    orc.head_fwd(qf, kf, vf, w.causal, w.scale, nthreads=nt)
+    orc.head_bwd(qf, kf, vf, dof, w.causal, w.scale, nthreads=nt)
+    return time.perf_counter() - t0, nt
+
+
+def cpu_baseline(w, q, k, v, do):
+    """The oracle timed on this host's cores: full fwd + bwd of whole heads
+    (exact outputs for those heads), ~10-30 s of CPU work."""
+    secs, flops, heads, nt = 0.0, 0.0, 0, 1
+    for head in range(w.B * w.H):
+        s, nt = run_oracle_sample(w, q, k, v, do, head, w.N)
+        secs += s
+        flops += oracle_head_flops(w, w.N)
+        heads += 1
+        if secs > 10.0:
+            break
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": nt, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of {heads} whole head(s) (N={w.N}, d={w.d}) of {w.name}, "
+                      f"{secs:.1f} s on {nt} threads ({cpu_model()})",
+            "seconds": secs}
+
+
+def reference_arm(args, w, rank: int, world: int):
+    """--impl reference: the oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return 0
+    from exact_attention_67_gb300.synth import make_inputs
+    q, k, v, do = make_inputs(w, with_grad=True)
+    # size each step's sample so that warmup + steps end within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = min(512, w.N)
+    s, _ = run_oracle_sample(w, q, k, v, do, 0, n_rows)
+    while n_rows * 2 <= w.N and s * 4.2 < budget:
+        n_rows *= 2
+        s, _ = run_oracle_sample(w, q, k, v, do, 0, n_rows)
+    for i in range(max(0, args.warmup - 1)):
+        run_oracle_sample(w, q, k, v, do, i % (w.B * w.H), n_rows)
+    total, nt = 0.0, 1
+    for i in range(args.steps):
+        s, nt = run_oracle_sample(w, q, k, v, do, i % (w.B * w.H), n_rows)
+        total += s
+    flops = oracle_head_flops(w, n_rows) * args.steps
+    value = flops / total / 1e12
+    sample = (f"per step: fp64 oracle fwd+bwd of the leading {n_rows}x{n_rows} block of one head of "
+              f"{w.name} (heads in turn); {nt} threads ({cpu_model()})")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, world: int):
+    return {"workload": f"{w.name} fwd+bwd" if w.bwd else f"{w.name} fwd",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": "1/sqrt(d)", "inputs": "bf16 N(0,1) (Q,K sigma %g), seeded" % w.sigma_qk,
+            "l2": "flushed before every step (256 MiB write, outside the timed events)",
+            "parallelism": "replicas" if world == 1 else f"replicas x{world} (independent heads per rank)"}
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse_args()
+    from exact_attention_67_gb300.synth import WORKLOADS
+    w = WORKLOADS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, w, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_67_gb300 as ex
+    from exact_attention_67_gb300 import build as exbuild
+    from exact_attention_67_gb300.synth import make_inputs
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        exbuild.build()
+    if world > 1:
+        dist.barrier()
+    ex.load()
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    q_h, k_h, v_h, do_h = make_inputs(w, seed_base=1000 * w.cfg + 100 * rank, with_grad=True)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    Dws = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    causal, scale = w.causal, w.scale
+    stream = torch.cuda.current_stream()
+
+    kernels = ["attn_fwd_kernel", "bwd_rowdot_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+
+    def step(evs):
+        evs[0].record(stream)
+        ex.attn_fwd(q, k, v, o, lse, causal, scale)
+        evs[1].record(stream)
+        ex.attn_bwd_preprocess(o, do, Dws)
+        evs[2].record(stream)
+        ex.attn_bwd_dkdv(q, k, v, do, lse, Dws, dk, dv, causal, scale)
+        evs[3].record(stream)
+        ex.attn_bwd_dq(q, k, v, do, lse, Dws, dq, causal, scale)
+        evs[4].record(stream)
+
+    def new_events(n):
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+
+    for evs in new_events(max(3, args.warmup)):
+        flush.zero_()
+        step(evs)
+    torch.cuda.synchronize()
+    if ex.device_error() != 0:
+        raise RuntimeError("kernel watchdog fired during warm-up")
+
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.3 if not args.no_clocks else 0.0)
+    ev = new_events(args.steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if ex.device_error() != 0:
+        raise RuntimeError("kernel watchdog fired during the timed region")
+
+    per_kernel = [0.0] * 4
+    for evs in ev:
+        for j in range(4):
+            per_kernel[j] += evs[j].elapsed_time(evs[j + 1])
+    total_ms = sum(per_kernel)
+    if world > 1:
+        t = torch.tensor([total_ms] + per_kernel, dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, per_kernel = float(t[0]), [float(x) for x in t[1:]]
+
+    F = w.flops_fwd()
+    steps = args.steps
+    t_fwd = per_kernel[0] / steps
+    t_bwd = sum(per_kernel[1:]) / steps
+    value = 3.5 * F * world / (total_ms / steps) / 1e9   # TFLOPS over all ranks
+    fwd_tflops = F / t_fwd / 1e9
+    bwd_tflops = 2.5 * F / t_bwd / 1e9
+    peak = peaks["bf16_tflops"]
+    # algorithmic FLOPs per launch: fwd = 2 GEMMs (QK^T, PV); dK/dV = 4 (S, dP, dV, dK);
+    # dQ = 1 (dQ; its S/dP recomputation is not counted); row dots: bytes only.
+    alg = {"attn_fwd_kernel": F, "bwd_rowdot_kernel": 0.0, "bwd_dkdv_kernel": 2.0 * F,
+           "bwd_dq_kernel": 0.5 * F}
+    rows = []
+    for name, ms in zip(kernels, per_kernel):
+        per = ms / steps
+        r = {"kernel": name, "ms": per, "share": ms / total_ms}
+        if alg[name] > 0:
+            r["tflops"] = alg[name] / per / 1e9
+            r["frac_of_peak"] = r["tflops"] / peak
+        else:
+            nbytes = 2 * 2 * w.B * w.H * w.N * w.d + 4 * w.B * w.H * w.N
+            r["gbs"] = nbytes / per / 1e6
+            r["frac_of_hbm"] = r["gbs"] / peaks["hbm_gbs"] if peaks["hbm_gbs"] else None
+        rows.append(r)
+    dom = max(range(4), key=lambda j: per_kernel[j])
+    dname = kernels[dom]
+    traffic = dram_traffic(dname, w.name)
+    roofline = {"bound": "tensor", "kernel": dname, "achieved": rows[dom].get("tflops"), "peak": peak,
+                "unit": "TFLOP/s", "frac": rows[dom].get("frac_of_peak"), "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                "algorithmic_flops_per_launch": alg[dname]}
+
+    # ---------------------------------------------------------------- e2e
+    e2e = None
+    if not args.no_e2e:
+        pin = [t.pin_memory() for t in (q_h, k_h, v_h, do_h)]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+        ws = torch.empty(ex.attn_bwd_workspace_size(w.B, w.H, w.N, w.d, causal), dtype=torch.uint8,
+                         device=dev)
+        dbuf = [torch.empty_like(t, device=dev) for t in pin]
+        n_e2e = max(3, min(steps, 20))
+
+        def e2e_step():
+            for src, dst in zip(pin, dbuf):
+                dst.copy_(src, non_blocking=True)
+            oo, ll = ex.forward(dbuf[0], dbuf[1], dbuf[2], causal, scale)
+            gq, gk, gv = ex.backward(dbuf[0], dbuf[1], dbuf[2], oo, ll, dbuf[3], causal, scale,
+                                     workspace=ws)
+            for src, dst in zip((oo, ll, gq, gk, gv), outs_h):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t[0])
+        h2d = sum(t.numel() * t.element_size() for t in pin)
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        e2e = {"value": 3.5 * F * world / ms / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n_e2e,
+               "path": "pinned host -> device copies, forward(), backward(), device -> pinned host copies"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q_h, k_h, v_h, do_h)
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, world),
+            "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+            "fwd_pct_peak": 100.0 * fwd_tflops / peak, "fwd_bwd_pct_peak": 100.0 * value / world / peak,
+            "kernels": rows, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * steps, "clocks": clocks,
+            "gpu": torch.cuda.get_device_name(dev)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
