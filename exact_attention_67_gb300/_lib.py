@@ -22,8 +22,8 @@ STATUS_NAMES = {
     7: "EXATTN_ERR_CUDA", 8: "EXATTN_ERR_TIMEOUT", 9: "EXATTN_ERR_VALUE",
 }
 # Every entry point include/exattn.h declares.
-EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "exattn_status_string",
-           "exattn_device_error", "exattn_version")
+EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
+           "attn_bwd_dq", "attn_bwd_noalloc", "exattn_status_string", "exattn_device_error", "exattn_version")
 
 
 class ExattnError(RuntimeError):
@@ -55,6 +55,14 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_fwd.restype = i
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
         lib.attn_bwd.restype = i
+        lib.attn_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        lib.attn_bwd_preprocess.restype = i
+        lib.attn_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.attn_bwd_dkdv.restype = i
+        lib.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.attn_bwd_dq.restype = i
+        lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.attn_bwd_noalloc.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.attn_bwd_workspace_size.restype = sz
         lib.exattn_status_string.argtypes = [i]
@@ -134,6 +142,44 @@ def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, worksp
     _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
                            _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), ws_bytes,
                            _stream(stream)))
+
+
+def _check_rows(t, shape, name):
+    if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous float32 {list(shape)}")
+
+
+def attn_bwd_preprocess(o, dO, D, stream=None) -> None:
+    """C ``attn_bwd_preprocess``: D (fp32 [B, H, N]) = rowsum(dO * O)."""
+    B, H, N, d = _shape4(o, "o")
+    if _shape4(dO, "dO") != (B, H, N, d):
+        raise ValueError("dO shape != o shape")
+    _check_rows(D, (B, H, N), "D")
+    _check(load().attn_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d, _stream(stream)))
+
+
+def attn_bwd_dkdv(q, k, v, dO, lse, D, dk, dv, causal: bool, scale: float, stream=None) -> None:
+    """C ``attn_bwd_dkdv``."""
+    B, H, N, d = _shape4(q, "q")
+    for n, t in (("k", k), ("v", v), ("dO", dO), ("dk", dk), ("dv", dv)):
+        if _shape4(t, n) != (B, H, N, d):
+            raise ValueError(f"{n} shape != q shape")
+    _check_rows(lse, (B, H, N), "lse")
+    _check_rows(D, (B, H, N), "D")
+    _check(load().attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dk), _ptr(dv),
+                                B, H, N, d, int(bool(causal)), float(scale), _stream(stream)))
+
+
+def attn_bwd_dq(q, k, v, dO, lse, D, dq, causal: bool, scale: float, stream=None) -> None:
+    """C ``attn_bwd_dq``."""
+    B, H, N, d = _shape4(q, "q")
+    for n, t in (("k", k), ("v", v), ("dO", dO), ("dq", dq)):
+        if _shape4(t, n) != (B, H, N, d):
+            raise ValueError(f"{n} shape != q shape")
+    _check_rows(lse, (B, H, N), "lse")
+    _check_rows(D, (B, H, N), "D")
+    _check(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq), B, H, N, d,
+                              int(bool(causal)), float(scale), _stream(stream)))
 
 
 def device_error() -> int:

@@ -105,6 +105,51 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
              size_t workspace_bytes, void* stream);
 
+/*
+ * The three stages of attn_bwd as separate calls, for callers that schedule
+ * them themselves (e.g. dK/dV and dQ on two streams once D is ready, or
+ * timing each kernel).  attn_bwd(...) equals attn_bwd_preprocess followed by
+ * attn_bwd_dkdv and attn_bwd_dq on one stream, with D in the workspace.
+ *
+ * attn_bwd_preprocess -- D[b,h,i] = sum_c dO[b,h,i,c] O[b,h,i,c], the
+ *   per-row term of the softmax gradient (dS_ij = P_ij (dP_ij - D_i)).
+ *   D: fp32 [B, H, N], 4-byte aligned, written.
+ * attn_bwd_dkdv -- dK and dV (bf16 [B, H, N, d], written) from q, k, v, dO,
+ *   lse (as written by attn_fwd) and D (from attn_bwd_preprocess).
+ * attn_bwd_dq   -- dQ (bf16 [B, H, N, d], written) from the same inputs.
+ * Validation, alignment and error codes as for attn_bwd.
+ */
+int attn_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d, void* stream);
+int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* D,
+                  void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* D,
+                void* dq, int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device
+ * memory: a plugin given only its input and output buffers by a runtime that
+ * owns all device memory, or code on a latency-critical path where an
+ * allocation (which may synchronise the device) is not allowed.  The pages
+ * this library follows have no counterpart of this call; it exists only for
+ * such callers.
+ *   Arguments, layout, results and errors are those of attn_bwd, without
+ *   the workspace: the row terms D_i live in a 16 MiB array built into the
+ *   library (fp32, one per query row), so B*H*N may be at most 4,194,304;
+ *   larger shapes return EXATTN_ERR_WORKSPACE without launching anything.
+ *   It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   The array occupies 16 MiB of device memory on every GPU that loads the
+ *   library, until the library is unloaded.  The first call on each device
+ *   looks up the array's device address (a runtime query, no allocation);
+ *   make that first call before any stream capture.  Every call shares the
+ *   array and it keeps the last call's contents (nothing in it needs to start
+ *   at zero: each call writes every D_i before reading it), so calls whose
+ *   executions overlap on the GPU (e.g. on two streams) race and must be
+ *   ordered by the caller.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                     float scale, void* stream);
+
 /* Human-readable text of an exattn_status (static storage, never NULL). */
 const char* exattn_status_string(int status);
 
