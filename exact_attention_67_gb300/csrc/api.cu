@@ -153,6 +153,101 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d, int causal
   return (rows * sizeof(float) + 255) & ~size_t(255);
 }
 
+namespace {
+
+// Shared set-up of the backward entry points (arguments already validated):
+// device state, the tensor maps of the given inputs (a null input skips its
+// maps), and the launch arguments.
+struct BwdMaps {
+  CUtensorMap m[8];
+};
+
+int bwd_setup(BwdArgs& a, BwdMaps& maps, const void* q, const void* k, const void* v, const void* dO, int B, int H,
+              int N, int d, int causal, float scale) {
+  int dev = 0;
+  unsigned* err = nullptr;
+  int rc = device_setup(&dev, &err);
+  if (rc != EXATTN_OK) return rc;
+  const int BH = B * H;
+  const void* src[4] = {q, k, v, dO};
+  for (int i = 0; i < 4; ++i) {
+    if (!src[i]) continue;
+    if (!make_map(&maps.m[i], src[i], BH, N, d, 128) || !make_map(&maps.m[4 + i], src[i], BH, N, d, 64))
+      return EXATTN_ERR_CUDA;
+  }
+  a.tm_q128 = &maps.m[0];
+  a.tm_k128 = &maps.m[1];
+  a.tm_v128 = &maps.m[2];
+  a.tm_do128 = &maps.m[3];
+  a.tm_q64 = &maps.m[4];
+  a.tm_k64 = &maps.m[5];
+  a.tm_v64 = &maps.m[6];
+  a.tm_do64 = &maps.m[7];
+  a.N = N;
+  a.BH = BH;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.err = err;
+  a.device = dev;
+  return EXATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
+                                   void* stream) {
+  if (!o || !dO || !D) return EXATTN_ERR_NULL;
+  int rc = check_common(B, H, N, d, 1.f);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(o, 16) || !aligned(dO, 16) || !aligned(D, 4)) return EXATTN_ERR_ALIGN;
+  BwdArgs a{};
+  BwdMaps maps;
+  if ((rc = bwd_setup(a, maps, nullptr, nullptr, nullptr, nullptr, B, H, N, d, 0, 1.f)) != EXATTN_OK) return rc;
+  a.o = o;
+  a.dO = dO;
+  a.D = D;
+  return launch_bwd_prep(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+}
+
+extern "C" int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                             const float* D, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                             void* stream) {
+  if (!q || !k || !v || !dO || !lse || !D || !dk || !dv) return EXATTN_ERR_NULL;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dO, 16) || !aligned(dk, 16) ||
+      !aligned(dv, 16) || !aligned(lse, 4) || !aligned(D, 4))
+    return EXATTN_ERR_ALIGN;
+  BwdArgs a{};
+  BwdMaps maps;
+  if ((rc = bwd_setup(a, maps, q, k, v, dO, B, H, N, d, causal, scale)) != EXATTN_OK) return rc;
+  a.lse = lse;
+  a.D = const_cast<float*>(D);
+  a.dk = dk;
+  a.dv = dv;
+  return launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+}
+
+extern "C" int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                           const float* D, void* dq, int B, int H, int N, int d, int causal, float scale,
+                           void* stream) {
+  if (!q || !k || !v || !dO || !lse || !D || !dq) return EXATTN_ERR_NULL;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dO, 16) || !aligned(dq, 16) ||
+      !aligned(lse, 4) || !aligned(D, 4))
+    return EXATTN_ERR_ALIGN;
+  BwdArgs a{};
+  BwdMaps maps;
+  if ((rc = bwd_setup(a, maps, q, k, v, dO, B, H, N, d, causal, scale)) != EXATTN_OK) return rc;
+  a.lse = lse;
+  a.D = const_cast<float*>(D);
+  a.dq = dq;
+  return launch_bwd_dq(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+}
+
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                         void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
                         void* workspace, size_t workspace_bytes, void* stream) {
@@ -164,28 +259,9 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     return EXATTN_ERR_ALIGN;
   if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, N, d, causal)) return EXATTN_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
-  int dev = 0;
-  unsigned* err = nullptr;
-  if ((rc = device_setup(&dev, &err)) != EXATTN_OK) return rc;
-  const int BH = B * H;
-  CUtensorMap m[8];
-  const void* src[4] = {q, k, v, dO};
-  for (int i = 0; i < 4; ++i) {
-    if (!make_map(&m[i], src[i], BH, N, d, 128) || !make_map(&m[4 + i], src[i], BH, N, d, 64))
-      return EXATTN_ERR_CUDA;
-  }
-  BwdArgs a;
-  a.tm_q128 = &m[0];
-  a.tm_k128 = &m[1];
-  a.tm_v128 = &m[2];
-  a.tm_do128 = &m[3];
-  a.tm_q64 = &m[4];
-  a.tm_k64 = &m[5];
-  a.tm_v64 = &m[6];
-  a.tm_do64 = &m[7];
-  a.q = q;
-  a.k = k;
-  a.v = v;
+  BwdArgs a{};
+  BwdMaps maps;
+  if ((rc = bwd_setup(a, maps, q, k, v, dO, B, H, N, d, causal, scale)) != EXATTN_OK) return rc;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
@@ -193,15 +269,11 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   a.dk = dk;
   a.dv = dv;
   a.D = static_cast<float*>(workspace);
-  a.N = N;
-  a.BH = BH;
-  a.d = d;
-  a.causal = causal ? 1 : 0;
-  a.scale = scale;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  a.err = err;
-  a.device = dev;
-  return launch_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_bwd_prep(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (launch_bwd_dkdv(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (launch_bwd_dq(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  return EXATTN_OK;
 }
 
 extern "C" const char* exattn_status_string(int status) {

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       const int s = it % C::STAGES;
       const uint32_t ph = (it / C::STAGES) & 1;
       if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
+      if (lane == 0) EXATTN_TRACE_POINT(0, it, 0);
       const int qi0 = (i_begin + it) * C::BR;
       float* st_lse2 = stat + s * 2 * C::BR;
       float* st_D = st_lse2 + C::BR;
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
           tma_load_3d(&tm_do, &bars->st_full[s], smem + C::OFF_DO + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, bh,
                       pol_keep);
         }
+        EXATTN_TRACE_POINT(0, it, 1);
       }
       issued = it + 1;
     }
@@ -224,11 +226,14 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         if (it + 1 < nq) {
           const int s1 = (it + 1) % C::STAGES;
           if (!(ok = mbar_wait(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1, wc))) break;
+          EXATTN_TRACE_POINT(1, it, 0);
           tc_fence_after();
           issue_products(it + 1);
           mma_commit(&bars->s_full[b ^ 1]);
+          EXATTN_TRACE_POINT(1, it, 1);
         }
         if (!(ok = mbar_wait(&bars->p_full[b], (it >> 1) & 1, wc))) break;
+        EXATTN_TRACE_POINT(1, it, 2);
         tc_fence_after();
         const uint32_t qa = q_base + s * C::QTILE, da = do_base + s * C::QTILE;
 #pragma unroll
@@ -240,6 +245,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
                  sdesc_sw128(qa + kk * 16 * 128, C::QCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->st_empty[s]);
+        EXATTN_TRACE_POINT(1, it, 3);
       }
       if (ok) mma_commit(&bars->acc_done);
       mma_commit(&bars->mma_done);
@@ -255,8 +261,10 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     for (int it = 0; ok && it < nq; ++it) {
       const int s = it % C::STAGES, b = it & 1;
       if (!(ok = mbar_wait(&bars->s_full[b], (it >> 1) & 1, wc))) break;
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 0);
       // The row statistics of this step were written by the producer's threads.
       if (!(ok = mbar_wait(&bars->st_full[s], (it / C::STAGES) & 1, wc))) break;
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 1);
       tc_fence_after();
       const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
       uint32_t sr[2][32], dr[2][32];
@@ -265,6 +273,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       tmem_ld32(tb + 64, dr[0]);
       tmem_ld32(tb + 96, dr[1]);
       tmem_wait_ld();
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 2);
       const float* st_lse2 = stat + s * 2 * C::BR;
       const float* st_D = st_lse2 + C::BR;
       const int qi0 = (i_begin + it) * C::BR;
@@ -290,6 +299,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         tmem_st16(tb + 64 + h * 16, dk_);   // dS^T over dP^T
       }
       tmem_wait_st();
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 3);
       tc_fence_before();
       mbar_arrive(&bars->p_full[b]);
     }
@@ -554,46 +564,55 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- launch
-template <int D, bool CAUSAL>
-static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
-  cudaError_t e;
-  {
-    const long long rows = static_cast<long long>(a.BH) * a.N;
-    const int rpb = 256 / (D / 8);  // rows per 256-thread block
-    long long blocks = (rows + rpb - 1) / rpb;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    bwd_rowdot_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.D, rows);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  {
-    using C = DkdvCfg<D>;
-    auto kern = bwd_dkdv_kernel<D, CAUSAL>;
-    if ((e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device)) != cudaSuccess)
-      return e;
-    const int n_kt = (a.N + C::BM - 1) / C::BM;
-    kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
-        static_cast<__nv_bfloat16*>(a.dv), a.N, a.BH, n_kt, a.scale, a.scale_log2, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  {
-    using C = DqCfg<D>;
-    auto kern = bwd_dq_kernel<D, CAUSAL>;
-    if ((e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device)) != cudaSuccess)
-      return e;
-    const int n_qt = (a.N + C::BM - 1) / C::BM;
-    kern<<<static_cast<unsigned>(static_cast<long long>(n_qt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.N, a.BH, n_qt,
-        a.scale, a.scale_log2, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+template <int D>
+static cudaError_t launch_prep_t(const BwdArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.BH) * a.N;
+  const int rpb = 256 / (D / 8);  // rows per 256-thread block
+  long long blocks = (rows + rpb - 1) / rpb;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  bwd_rowdot_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.D, rows);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
-  return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+template <int D, bool CAUSAL>
+static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = DkdvCfg<D>;
+  auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
+  if (e != cudaSuccess) return e;
+  const int n_kt = (a.N + C::BM - 1) / C::BM;
+  kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
+      *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
+      static_cast<__nv_bfloat16*>(a.dv), a.N, a.BH, n_kt, a.scale, a.scale_log2, a.err);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = DqCfg<D>;
+  auto kern = bwd_dq_kernel<D, CAUSAL>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (a.N + C::BM - 1) / C::BM;
+  kern<<<static_cast<unsigned>(static_cast<long long>(n_qt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
+      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.N, a.BH,
+      n_qt, a.scale, a.scale_log2, a.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_prep_t<64>(a, stream) : launch_prep_t<128>(a, stream);
+}
+
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_dkdv_t<64, true>(a, stream) : launch_dkdv_t<64, false>(a, stream);
+  return a.causal ? launch_dkdv_t<128, true>(a, stream) : launch_dkdv_t<128, false>(a, stream);
+}
+
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_dq_t<64, true>(a, stream) : launch_dq_t<64, false>(a, stream);
+  return a.causal ? launch_dq_t<128, true>(a, stream) : launch_dq_t<128, false>(a, stream);
 }
 
 }  // namespace exattn

@@ -47,6 +47,8 @@ struct BwdArgs {
 
 cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace exattn

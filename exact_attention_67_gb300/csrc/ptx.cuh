@@ -31,6 +31,23 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
+// Timeline instrumentation, compiled out unless EXATTN_TRACE is defined: a
+// tracing build (which defines the two device variables below) records
+// clock64() at named points of one selected CTA, slot [role][iteration][event].
+#ifdef EXATTN_TRACE
+extern __device__ unsigned long long* g_exattn_trace;
+extern __device__ int g_exattn_trace_cta;
+#define EXATTN_TRACE_POINT(role, it, ev)                                                   \
+  do {                                                                                    \
+    if (static_cast<int>(blockIdx.x) == g_exattn_trace_cta && (it) < 256)                  \
+      g_exattn_trace[((role) * 256 + (it)) * 8 + (ev)] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+#else
+#define EXATTN_TRACE_POINT(role, it, ev) \
+  do {                                   \
+  } while (0)
+#endif
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -121,3 +121,24 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "library_path", lambda: str(tmp_path / "nope.so"))
     with pytest.raises(ImportError):
         _lib.load()
+
+
+def test_stage_validation(lib):
+    # attn_bwd_preprocess(o, dO, D, B, H, N, d, stream)
+    assert lib.attn_bwd_preprocess(None, P[1], P[2], 1, 1, 8, 64, None) == 1
+    assert lib.attn_bwd_preprocess(P[0], P[1], P[2], 1, 1, 0, 64, None) == 2
+    assert lib.attn_bwd_preprocess(P[0], P[1], P[2], 1, 1, 8, 48, None) == 4
+    assert lib.attn_bwd_preprocess(P[0] + 2, P[1], P[2], 1, 1, 8, 64, None) == 3
+    assert lib.attn_bwd_preprocess(P[0], P[1], P[2] + 2, 1, 1, 8, 64, None) == 3
+    # attn_bwd_dkdv(q, k, v, dO, lse, D, dk, dv, B, H, N, d, causal, scale, stream)
+    args = list(P[:8])
+    assert lib.attn_bwd_dkdv(*args[:5], None, *args[6:8], 1, 1, 8, 64, 0, 0.1, None) == 1
+    assert lib.attn_bwd_dkdv(*args, 1, 1, 8, 64, 0, 0.0, None) == 9
+    bad = list(args)
+    bad[6] += 8
+    assert lib.attn_bwd_dkdv(*bad, 1, 1, 8, 64, 0, 0.1, None) == 3
+    # attn_bwd_dq(q, k, v, dO, lse, D, dq, B, H, N, d, causal, scale, stream)
+    args = list(P[:7])
+    assert lib.attn_bwd_dq(*args[:6], None, 1, 1, 8, 64, 0, 0.1, None) == 1
+    assert lib.attn_bwd_dq(*args, 1, 1, 8, 128, 1, float("inf"), None) == 9
+    assert lib.attn_bwd_dq(*args, -1, 1, 8, 128, 1, 0.1, None) == 2
