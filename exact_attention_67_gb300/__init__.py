@@ -11,11 +11,12 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (EXPORTS, ExattnError, attn_bwd, attn_bwd_workspace_size, attn_fwd, device_error,
-                   library_path, load, status_string, version)
+from ._lib import (EXPORTS, ExattnError, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_preprocess,
+                   attn_bwd_workspace_size, attn_fwd, device_error, library_path, load, status_string, version)
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "forward", "backward", "device_error",
-           "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
+           "attn_bwd_dq", "forward", "backward", "device_error", "status_string", "version", "load",
+           "library_path", "ExattnError", "EXPORTS"]
 
 
 def _default_scale(d: int) -> float:

@@ -71,7 +71,7 @@ struct DkdvCfg {
   static constexpr int QCHUNK = BR * 128;  // ... of a 64-row tile
   static constexpr int KTILE = NCHUNK * KCHUNK;
   static constexpr int QTILE = NCHUNK * QCHUNK;
-  static constexpr int STAGES = (D == 64) ? 4 : 3;
+  static constexpr int STAGES = (D == 64) ? 6 : 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KTILE;
   static constexpr int OFF_Q = OFF_V + KTILE;
@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
   float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  EXATTN_TRACE_INIT();
 
   // Under the causal mask the first key tiles meet the most queries: run them first.
   const int kt = static_cast<int>(blockIdx.x) / BH;
@@ -157,22 +158,36 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         tma_load_3d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, k0, bh, pol_keep);
       }
     }
+    // Row terms of the next step are fetched into registers one step ahead, so
+    // their global-load latency overlaps the wait for a free stage.
+    auto fetch_terms = [&](int it, float (&l2)[2], float (&dd)[2]) {
+      const int qi0 = (i_begin + it) * C::BR;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int qi = qi0 + lane + 32 * u;
+        const bool valid = it < nq && qi < N;
+        // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
+        l2[u] = valid ? lse[static_cast<size_t>(bh) * N + qi] * kLog2e : INFINITY;
+        dd[u] = valid ? Dws[static_cast<size_t>(bh) * N + qi] : 0.f;
+      }
+    };
+    float nl2[2], ndd[2];
+    fetch_terms(0, nl2, ndd);
     int issued = 0;
     for (int it = 0; it < nq; ++it) {
       const int s = it % C::STAGES;
       const uint32_t ph = (it / C::STAGES) & 1;
+      const float l2a = nl2[0], l2b = nl2[1], dda = ndd[0], ddb = ndd[1];
+      fetch_terms(it + 1, nl2, ndd);
       if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
       if (lane == 0) EXATTN_TRACE_POINT(0, it, 0);
       const int qi0 = (i_begin + it) * C::BR;
       float* st_lse2 = stat + s * 2 * C::BR;
       float* st_D = st_lse2 + C::BR;
-      for (int e = lane; e < C::BR; e += 32) {
-        const int qi = qi0 + e;
-        const bool valid = qi < N;
-        // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
-        st_lse2[e] = valid ? lse[static_cast<size_t>(bh) * N + qi] * kLog2e : INFINITY;
-        st_D[e] = valid ? Dws[static_cast<size_t>(bh) * N + qi] : 0.f;
-      }
+      st_lse2[lane] = l2a;
+      st_lse2[lane + 32] = l2b;
+      st_D[lane] = dda;
+      st_D[lane + 32] = ddb;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QTILE);
@@ -194,63 +209,78 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, C::BR, 0, 0);  // K (or V) x Q^T (or dO^T): both K-major
-      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);    // TMEM operand x (Q or dO), MN-major
-      const uint32_t k_base = smem_u32(smem + C::OFF_K);
-      const uint32_t v_base = smem_u32(smem + C::OFF_V);
-      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-      const uint32_t do_base = smem_u32(smem + C::OFF_DO);
-      auto issue_products = [&](int it) {
-        const int s = it % C::STAGES, b = it & 1;
-        const uint32_t qa = q_base + s * C::QTILE, da = do_base + s * C::QTILE;
+    // Whole-warp loop, elected lane issues (see elect_one()).
+    constexpr uint32_t idesc_s = idesc_bf16(128, C::BR, 0, 0);  // K (or V) x Q^T (or dO^T): both K-major
+    constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);    // TMEM operand x (Q or dO), MN-major
+    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+    const uint64_t q_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::QCHUNK, 1024);
+    const uint64_t do_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::QCHUNK, 1024);
+    constexpr uint32_t kQTileDesc = C::QTILE >> 4;
+    auto issue_products = [&](int it) {
+      const int s = it % C::STAGES, b = it & 1;
+      const uint64_t qa = q_desc + s * kQTileDesc, da = do_desc + s * kQTileDesc;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
-          const uint32_t qo = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_BUF + b * 128, sdesc_sw128(k_base + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024),
-                 idesc_s, kk > 0);
-          mma_ss(tmem + C::TM_BUF + b * 128 + 64, sdesc_sw128(v_base + ko, 16, 1024),
-                 sdesc_sw128(da + qo, 16, 1024), idesc_s, kk > 0);
-        }
-      };
-      bool ok = mbar_wait(&bars->kv_full, 0, wc);
-      if (ok) ok = mbar_wait(&bars->st_full[0], 0, wc);
-      if (ok) {
-        tc_fence_after();
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
+        const uint32_t qo = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
+        mma_ss(tmem + C::TM_BUF + b * 128, k_desc + ko, qa + qo, idesc_s, kk > 0);
+        mma_ss(tmem + C::TM_BUF + b * 128 + 64, v_desc + ko, da + qo, idesc_s, kk > 0);
+      }
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    };
+    bool ok = wait_all(&bars->kv_full, 0);
+    if (ok) ok = wait_all(&bars->st_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
         issue_products(0);
         mma_commit(&bars->s_full[0]);
       }
-      for (int it = 0; ok && it < nq; ++it) {
-        const int s = it % C::STAGES, b = it & 1;
-        if (it + 1 < nq) {
-          const int s1 = (it + 1) % C::STAGES;
-          if (!(ok = mbar_wait(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1, wc))) break;
-          EXATTN_TRACE_POINT(1, it, 0);
-          tc_fence_after();
+      __syncwarp();
+    }
+    for (int it = 0; ok && it < nq; ++it) {
+      const int s = it % C::STAGES, b = it & 1;
+      if (it + 1 < nq) {
+        const int s1 = (it + 1) % C::STAGES;
+        if (!(ok = wait_all(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1))) break;
+        if (lane == 0) EXATTN_TRACE_POINT(1, it, 0);
+        tc_fence_after();
+        if (elect_one()) {
           issue_products(it + 1);
           mma_commit(&bars->s_full[b ^ 1]);
-          EXATTN_TRACE_POINT(1, it, 1);
         }
-        if (!(ok = mbar_wait(&bars->p_full[b], (it >> 1) & 1, wc))) break;
-        EXATTN_TRACE_POINT(1, it, 2);
-        tc_fence_after();
-        const uint32_t qa = q_base + s * C::QTILE, da = do_base + s * C::QTILE;
+        __syncwarp();
+        if (lane == 0) EXATTN_TRACE_POINT(1, it, 1);
+      }
+      if (!(ok = wait_all(&bars->p_full[b], (it >> 1) & 1))) break;
+      if (lane == 0) EXATTN_TRACE_POINT(1, it, 2);
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t qa = q_mn + s * kQTileDesc, da = do_mn + s * kQTileDesc;
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {
           // dV += P^T dO_i ; dK += dS^T Q_i  (operands over the first 32 columns of S^T / dP^T)
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_BUF + b * 128 + kk * 8,
-                 sdesc_sw128(da + kk * 16 * 128, C::QCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + kk * 8,
-                 sdesc_sw128(qa + kk * 16 * 128, C::QCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_BUF + b * 128 + kk * 8, da + ((kk * 16 * 128) >> 4), idesc_acc, acc);
+          mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + kk * 8, qa + ((kk * 16 * 128) >> 4), idesc_acc,
+                 acc);
         }
         mma_commit(&bars->st_empty[s]);
-        EXATTN_TRACE_POINT(1, it, 3);
       }
+      __syncwarp();
+      if (lane == 0) EXATTN_TRACE_POINT(1, it, 3);
+    }
+    if (elect_one()) {
       if (ok) mma_commit(&bars->acc_done);
       mma_commit(&bars->mma_done);
-      mbar_wait_drain(&bars->mma_done, 0, err);
     }
+    __syncwarp();
+    if (lane == 0) mbar_wait_drain(&bars->mma_done, 0, err);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise (thread = key row)
@@ -348,7 +378,7 @@ struct DqCfg {
   static constexpr int KCHUNK = BN * 128;
   static constexpr int QTILE = NCHUNK * QCHUNK;
   static constexpr int KTILE = NCHUNK * KCHUNK;
-  static constexpr int STAGES = (D == 64) ? 4 : 3;
+  static constexpr int STAGES = (D == 64) ? 6 : 4;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + QTILE;
   static constexpr int OFF_K = OFF_DO + QTILE;
@@ -372,6 +402,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  EXATTN_TRACE_INIT();
 
   // Under the causal mask the last query tiles meet the most keys: run them first.
   const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.x) / BH;
@@ -438,55 +469,69 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 5) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);
-      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-      const uint32_t do_base = smem_u32(smem + C::OFF_DO);
-      const uint32_t k_base = smem_u32(smem + C::OFF_K);
-      const uint32_t v_base = smem_u32(smem + C::OFF_V);
-      auto issue_products = [&](int it) {
-        const int s = it % C::STAGES, b = it & 1;
-        const uint32_t ka = k_base + s * C::KTILE, va = v_base + s * C::KTILE;
+    // Whole-warp loop, elected lane issues (see elect_one()).
+    constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);
+    constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
+    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::KCHUNK, 1024);
+    constexpr uint32_t kKTileDesc = C::KTILE >> 4;
+    auto issue_products = [&](int it) {
+      const int s = it % C::STAGES, b = it & 1;
+      const uint64_t ka = k_desc + s * kKTileDesc, va = v_desc + s * kKTileDesc;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_BUF + b * 128, sdesc_sw128(q_base + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024),
-                 idesc_s, kk > 0);
-          mma_ss(tmem + C::TM_BUF + b * 128 + 64, sdesc_sw128(do_base + qo, 16, 1024),
-                 sdesc_sw128(va + ko, 16, 1024), idesc_s, kk > 0);
-        }
-      };
-      bool ok = mbar_wait(&bars->kv_full, 0, wc);
-      if (ok) ok = mbar_wait(&bars->st_full[0], 0, wc);
-      if (ok) {
-        tc_fence_after();
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
+        const uint32_t ko = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
+        mma_ss(tmem + C::TM_BUF + b * 128, q_desc + qo, ka + ko, idesc_s, kk > 0);
+        mma_ss(tmem + C::TM_BUF + b * 128 + 64, do_desc + qo, va + ko, idesc_s, kk > 0);
+      }
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    };
+    bool ok = wait_all(&bars->kv_full, 0);
+    if (ok) ok = wait_all(&bars->st_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
         issue_products(0);
         mma_commit(&bars->s_full[0]);
       }
-      for (int it = 0; ok && it < nk; ++it) {
-        const int s = it % C::STAGES, b = it & 1;
-        if (it + 1 < nk) {
-          const int s1 = (it + 1) % C::STAGES;
-          if (!(ok = mbar_wait(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1, wc))) break;
-          tc_fence_after();
+      __syncwarp();
+    }
+    for (int it = 0; ok && it < nk; ++it) {
+      const int s = it % C::STAGES, b = it & 1;
+      if (it + 1 < nk) {
+        const int s1 = (it + 1) % C::STAGES;
+        if (!(ok = wait_all(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1))) break;
+        tc_fence_after();
+        if (elect_one()) {
           issue_products(it + 1);
           mma_commit(&bars->s_full[b ^ 1]);
         }
-        if (!(ok = mbar_wait(&bars->p_full[b], (it >> 1) & 1, wc))) break;
-        tc_fence_after();
-        const uint32_t ka = k_base + s * C::KTILE;
+        __syncwarp();
+      }
+      if (!(ok = wait_all(&bars->p_full[b], (it >> 1) & 1))) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t ka = k_mn + s * kKTileDesc;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::TM_DQ, tmem + C::TM_BUF + b * 128 + kk * 8,
-                 sdesc_sw128(ka + kk * 16 * 128, C::KCHUNK, 1024), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::TM_DQ, tmem + C::TM_BUF + b * 128 + kk * 8, ka + ((kk * 16 * 128) >> 4), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->st_empty[s]);
       }
+      __syncwarp();
+    }
+    if (elect_one()) {
       if (ok) mma_commit(&bars->acc_done);
       mma_commit(&bars->mma_done);
-      mbar_wait_drain(&bars->mma_done, 0, err);
     }
+    __syncwarp();
+    if (lane == 0) mbar_wait_drain(&bars->mma_done, 0, err);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise (thread = query row)

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  EXATTN_TRACE_INIT();
 
   // Heaviest work first: under the causal mask the last query pairs see the most keys.
   const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
@@ -139,12 +140,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
         if (!mbar_wait(&bars->k_empty[s], ph ^ 1, wc)) break;
+        EXATTN_TRACE_POINT(0, j, 0);
         mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(&tm_k, &bars->k_full[s], smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
                       j * C::BN, bh, pol_kv);
         issued_k = j + 1;
         if (!mbar_wait(&bars->v_empty[s], ph ^ 1, wc)) break;
+        EXATTN_TRACE_POINT(0, j, 1);
         mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(&tm_v, &bars->v_full[s], smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
@@ -164,80 +167,101 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);  // Q, K both K-major
-      constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);      // P from TMEM, V MN-major
-      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-      const uint32_t k_base = smem_u32(smem + C::OFF_K);
-      const uint32_t v_base = smem_u32(smem + C::OFF_V);
+    // The whole warp runs this loop (waits and descriptor arithmetic stay
+    // warp-uniform); the elected lane issues the tcgen05 instructions.
+    constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);  // Q, K both K-major
+    constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);      // P from TMEM, V MN-major
+    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::CHUNK_BYTES, 1024);
+    constexpr uint32_t kTileDesc = C::TILE_BYTES >> 4;  // descriptor units are 16 bytes
 
-      auto issue_s = [&](int t, int stage) {
-        const uint32_t qa = q_base + t * C::TILE_BYTES;
-        const uint32_t ka = k_base + stage * C::TILE_BYTES;
+    auto issue_s = [&](int t, int stage) {
+      const uint64_t a = q_desc + t * kTileDesc, b = k_desc + stage * kTileDesc;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_S + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 idesc_s, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int t, int stage, bool acc) {
-        const uint32_t va = v_base + stage * C::TILE_BYTES;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+        mma_ss(tmem + C::TM_S + t * 128, a + off, b + off, idesc_s, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int t, int stage, bool acc) {
+      const uint64_t b = v_desc + stage * kTileDesc;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          mma_ts(tmem + C::TM_O + t * 128, tmem + C::TM_S + t * 128 + kk * 8,
-                 sdesc_sw128(va + kk * 16 * 128, C::CHUNK_BYTES, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_ts(tmem + C::TM_O + t * 128, tmem + C::TM_S + t * 128 + kk * 8, b + ((kk * 16 * 128) >> 4), idesc_o,
+               (acc || kk > 0) ? 1u : 0u);
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    };
 
-      bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if ((t == 0 ? nkv0 : nkv1) > 0) ok = mbar_wait(&bars->q_full[t], 0, wc);
-      if (ok && n_iter > 0) ok = mbar_wait(&bars->k_full[0], 0, wc);
-      if (ok && n_iter > 0) {
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if ((t == 0 ? nkv0 : nkv1) == 0) continue;
-          issue_s(t, 0);
-          mma_commit(&bars->s_full[t]);
+    bool ok = true;
+    if (nkv0 > 0) ok = wait_all(&bars->q_full[0], 0);
+    if (ok && nkv1 > 0) ok = wait_all(&bars->q_full[1], 0);
+    if (ok && n_iter > 0) ok = wait_all(&bars->k_full[0], 0);
+    if (ok && n_iter > 0) {
+      tc_fence_after();
+      if (elect_one()) {
+        if (nkv0 > 0) {
+          issue_s(0, 0);
+          mma_commit(&bars->s_full[0]);
+        }
+        if (nkv1 > 0) {
+          issue_s(1, 0);
+          mma_commit(&bars->s_full[1]);
         }
         mma_commit(&bars->k_empty[0]);
       }
-      for (int j = 0; ok && j < n_iter; ++j) {
-        const int s = j % C::STAGES;
-        const uint32_t ph = (j / C::STAGES) & 1;
-        const int s1 = (j + 1) % C::STAGES;
-        const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
-        bool v_ready = false, k_ready = false;
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_iter; ++j) {
+      const int s = j % C::STAGES;
+      const uint32_t ph = (j / C::STAGES) & 1;
+      const int s1 = (j + 1) % C::STAGES;
+      const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+      bool v_ready = false, k_ready = false;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || j >= (t == 0 ? nkv0 : nkv1)) continue;
-          if (!(ok = mbar_wait(&bars->p_full[t], j & 1, wc))) continue;
-          if (!v_ready) {
-            if (!(ok = mbar_wait(&bars->v_full[s], ph, wc))) continue;
-            v_ready = true;
+      for (int t = 0; t < 2; ++t) {
+        const int nkv_t = t == 0 ? nkv0 : nkv1;
+        if (!ok || j >= nkv_t) continue;
+        if (!(ok = wait_all(&bars->p_full[t], j & 1))) continue;
+        if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 0);
+        if (!v_ready) {
+          if (!(ok = wait_all(&bars->v_full[s], ph))) continue;
+          v_ready = true;
+        }
+        if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 1);
+        tc_fence_after();
+        if (elect_one()) issue_pv(t, s, j > 0);
+        __syncwarp();
+        if (j + 1 < nkv_t) {
+          if (!k_ready) {
+            if (!(ok = wait_all(&bars->k_full[s1], ph1))) continue;
+            k_ready = true;
+            tc_fence_after();
           }
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          if (j + 1 < (t == 0 ? nkv0 : nkv1)) {
-            if (!k_ready) {
-              if (!(ok = mbar_wait(&bars->k_full[s1], ph1, wc))) continue;
-              k_ready = true;
-              tc_fence_after();
-            }
+          if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 2);
+          if (elect_one()) {
             issue_s(t, s1);
             mma_commit(&bars->s_full[t]);
-          } else {
-            mma_commit(&bars->o_full[t]);
           }
+          __syncwarp();
+          if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 3);
+        } else {
+          if (elect_one()) mma_commit(&bars->o_full[t]);
+          __syncwarp();
         }
+      }
+      if (elect_one()) {
         if (v_ready) mma_commit(&bars->v_empty[s]);
         if (k_ready) mma_commit(&bars->k_empty[s1]);
       }
-      // Nothing may still read shared memory or write TMEM once the CTA tears down.
-      mma_commit(&bars->mma_done);
-      mbar_wait_drain(&bars->mma_done, 0, err);
+      __syncwarp();
     }
+    // Nothing may still read shared memory or write TMEM once the CTA tears down.
+    if (elect_one()) mma_commit(&bars->mma_done);
+    __syncwarp();
+    if (lane == 0) mbar_wait_drain(&bars->mma_done, 0, err);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
@@ -253,6 +277,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     bool ok = (t == 0 ? nkv0 : nkv1) > 0;
     for (int j = 0; ok && j < (t == 0 ? nkv0 : nkv1); ++j) {
       if (!(ok = mbar_wait(&bars->s_full[t], j & 1, wc))) break;
+      if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 0);
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
@@ -322,6 +347,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
+      if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 1);
       mbar_arrive(&bars->p_full[t]);
     }
     // ---------------------------------------------------------- epilogue

@@ -32,21 +32,42 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 
 // Timeline instrumentation, compiled out unless EXATTN_TRACE is defined: a
-// tracing build (which defines the two device variables below) records
-// clock64() at named points of one selected CTA, slot [role][iteration][event].
+// tracing build, which defines exattn::g_exattn_trace (unsigned long long*)
+// and exattn::g_exattn_trace_cta (int) as __device__ variables before
+// including the kernels, records clock64() at named points of one selected
+// CTA into slot [role][iteration][event].  EXATTN_TRACE_INIT() at kernel entry
+// reads the selection once, so a trace point costs one store.
 #ifdef EXATTN_TRACE
-extern __device__ unsigned long long* g_exattn_trace;
-extern __device__ int g_exattn_trace_cta;
-#define EXATTN_TRACE_POINT(role, it, ev)                                                   \
-  do {                                                                                    \
-    if (static_cast<int>(blockIdx.x) == g_exattn_trace_cta && (it) < 256)                  \
-      g_exattn_trace[((role) * 256 + (it)) * 8 + (ev)] = static_cast<unsigned long long>(clock64()); \
+#define EXATTN_TRACE_INIT()                                                          \
+  unsigned long long* const exattn_trace_buf =                                       \
+      (static_cast<int>(blockIdx.x) == g_exattn_trace_cta) ? g_exattn_trace : nullptr
+#define EXATTN_TRACE_POINT(role, it, ev)                                                             \
+  do {                                                                                              \
+    if (exattn_trace_buf != nullptr && (it) < 256)                                                 \
+      exattn_trace_buf[((role) * 256 + (it)) * 8 + (ev)] = static_cast<unsigned long long>(clock64()); \
   } while (0)
 #else
+#define EXATTN_TRACE_INIT() \
+  do {                      \
+  } while (0)
 #define EXATTN_TRACE_POINT(role, it, ev) \
   do {                                   \
   } while (0)
 #endif
+
+// One lane of a converged warp (elect.sync).  MMA-issuing code runs its loop
+// with the whole warp, so that addresses and descriptors stay warp-uniform,
+// and issues each tcgen05 instruction from the elected lane only: one thread
+// looping alone issues an MMA every ~70 cycles, the elected form every ~25.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
