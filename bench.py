@@ -57,6 +57,23 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
+def max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over all ranks of the default
+    process group (the slowest rank's times); the identity without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return flops_per_rank * world / ms / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -343,17 +360,14 @@ def main():
     for evs in ev:
         for j in range(4):
             per_kernel[j] += evs[j].elapsed_time(evs[j + 1])
-    total_ms = sum(per_kernel)
-    if world > 1:
-        t = torch.tensor([total_ms] + per_kernel, dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, per_kernel = float(t[0]), [float(x) for x in t[1:]]
+    reduced = max_over_ranks([sum(per_kernel)] + per_kernel, dev)
+    total_ms, per_kernel = reduced[0], reduced[1:]
 
     F = w.flops_fwd()
     steps = args.steps
     t_fwd = per_kernel[0] / steps
     t_bwd = sum(per_kernel[1:]) / steps
-    value = 3.5 * F * world / (total_ms / steps) / 1e9   # TFLOPS over all ranks
+    value = job_tflops(3.5 * F, world, total_ms / steps)   # TFLOPS over all ranks
     fwd_tflops = F / t_fwd / 1e9
     bwd_tflops = 2.5 * F / t_bwd / 1e9
     peak = peaks["bf16_tflops"]
@@ -411,14 +425,10 @@ def main():
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t[0])
+        ms = max_over_ranks([e0.elapsed_time(e1) / n_e2e], dev)[0]
         h2d = sum(t.numel() * t.element_size() for t in pin)
         d2h = sum(t.numel() * t.element_size() for t in outs_h)
-        e2e = {"value": 3.5 * F * world / ms / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_tflops(3.5 * F, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n_e2e,
                "path": "pinned host -> device copies, forward(), backward(), device -> pinned host copies"}
 

@@ -23,7 +23,8 @@ STATUS_NAMES = {
 }
 # Every entry point include/exattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_bwd_noalloc", "exattn_status_string", "exattn_device_error", "exattn_version")
+           "attn_bwd_dq", "attn_bwd_noalloc", "exattn_status_string", "exattn_device_error",
+           "exattn_watchdog_selftest", "exattn_version")
 
 
 class ExattnError(RuntimeError):
@@ -69,6 +70,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.exattn_status_string.restype = ctypes.c_char_p
         lib.exattn_device_error.argtypes = []
         lib.exattn_device_error.restype = i
+        lib.exattn_watchdog_selftest.argtypes = [ctypes.c_uint, vp]
+        lib.exattn_watchdog_selftest.restype = i
         lib.exattn_version.argtypes = []
         lib.exattn_version.restype = i
         _lib = lib
@@ -185,6 +188,11 @@ def attn_bwd_dq(q, k, v, dO, lse, D, dq, causal: bool, scale: float, stream=None
 def device_error() -> int:
     """Synchronise and read/clear the kernels' watchdog word (0 = clean)."""
     return int(load().exattn_device_error())
+
+
+def watchdog_selftest(timeout_us: int = 2000, stream=None) -> None:
+    """C ``exattn_watchdog_selftest``: a deliberately unsatisfied bounded wait."""
+    _check(load().exattn_watchdog_selftest(int(timeout_us), _stream(stream)))
 
 
 def version() -> int:

@@ -9,11 +9,29 @@
 
 #include "exattn.h"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace exattn {
 
 // Watchdog word shared by every kernel launch on a device (bit flags from ptx.cuh).
 __device__ unsigned g_err_word;
+
+// One warp waits on an mbarrier that nothing ever arrives on, with the given
+// limit: the bounded wait gives up, reports through the watchdog word and the
+// kernel returns normally.  Used to check the failure path end to end.
+__global__ void watchdog_selftest_kernel(unsigned long long limit_ns, unsigned* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const WaitCtl wc{&abort_flag, err};
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, wc, limit_ns);
+  __syncwarp();
+}
 
 namespace {
 
@@ -306,6 +324,16 @@ extern "C" int exattn_device_error(void) {
     return EXATTN_ERR_TIMEOUT;
   }
   return EXATTN_OK;
+}
+
+extern "C" int exattn_watchdog_selftest(unsigned timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return EXATTN_ERR_VALUE;
+  int dev = 0;
+  unsigned* err = nullptr;
+  int rc = device_setup(&dev, &err);
+  if (rc != EXATTN_OK) return rc;
+  watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1000ull * timeout_us, err);
+  return cudaGetLastError() == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
 extern "C" int exattn_version(void) { return 100; }

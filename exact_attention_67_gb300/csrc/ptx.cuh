@@ -107,7 +107,8 @@ struct WaitCtl {
 
 // Wait until the phase with the given parity of `bar` has completed.
 // Returns false (and raises the CTA abort flag) if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
@@ -121,7 +122,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
         *w.abort = 1;
         return false;
       }
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *w.abort = 1;
         atomicOr(w.err, kErrWaitTimeout);
         return false;

@@ -161,6 +161,18 @@ const char* exattn_status_string(int status);
  */
 int exattn_device_error(void);
 
+/*
+ * exattn_watchdog_selftest -- exercises the failure path of the kernels'
+ * bounded waits without any fault: launches one warp that waits on a
+ * barrier nothing arrives on, giving up after timeout_us microseconds
+ * (1..1,000,000).  The next exattn_device_error() then returns
+ * EXATTN_ERR_TIMEOUT (and clears the word); the context stays usable.
+ * While the word is set, waits in other launches that have to spin give up
+ * early, so read it before launching real work.  Returns EXATTN_ERR_VALUE
+ * for a timeout out of range.
+ */
+int exattn_watchdog_selftest(unsigned timeout_us, void* stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int exattn_version(void);
 
