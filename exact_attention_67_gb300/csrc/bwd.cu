@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const int s = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1;
         if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
+        EXATTN_TRACE_POINT(0, it, 0);
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_3d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
@@ -507,14 +508,17 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       if (it + 1 < nk) {
         const int s1 = (it + 1) % C::STAGES;
         if (!(ok = wait_all(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1))) break;
+        if (lane == 0) EXATTN_TRACE_POINT(1, it, 0);
         tc_fence_after();
         if (elect_one()) {
           issue_products(it + 1);
           mma_commit(&bars->s_full[b ^ 1]);
         }
         __syncwarp();
+        if (lane == 0) EXATTN_TRACE_POINT(1, it, 1);
       }
       if (!(ok = wait_all(&bars->p_full[b], (it >> 1) & 1))) break;
+      if (lane == 0) EXATTN_TRACE_POINT(1, it, 2);
       tc_fence_after();
       if (elect_one()) {
         const uint64_t ka = k_mn + s * kKTileDesc;
@@ -525,6 +529,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mma_commit(&bars->st_empty[s]);
       }
       __syncwarp();
+      if (lane == 0) EXATTN_TRACE_POINT(1, it, 3);
     }
     if (elect_one()) {
       if (ok) mma_commit(&bars->acc_done);
@@ -546,6 +551,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     for (int it = 0; ok && it < nk; ++it) {
       const int b = it & 1;
       if (!(ok = mbar_wait(&bars->s_full[b], (it >> 1) & 1, wc))) break;
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 0);
       tc_fence_after();
       const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
       uint32_t sr[2][32], dr[2][32];
@@ -554,6 +560,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tmem_ld32(tb + 64, dr[0]);
       tmem_ld32(tb + 96, dr[1]);
       tmem_wait_ld();
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 2);
       const int kj0 = it * C::BN;
       const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > q0) || (kj0 + C::BN > N);
       int lim = N - kj0;
@@ -576,6 +583,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         tmem_st16(tb + h * 16, pk);  // dS over S
       }
       tmem_wait_st();
+      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 3);
       tc_fence_before();
       mbar_arrive(&bars->p_full[b]);
     }
