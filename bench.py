@@ -88,7 +88,7 @@ def load_peaks():
 
 
 def kernel_source_sha(name: str) -> str:
-    src = {"attn_fwd_kernel": "fwd.cu", "bwd_dkdv_kernel": "bwd.cu", "bwd_dq_kernel": "bwd.cu",
+    src = {"attn_fwd_kernel": "fwd.cu", "bwd_dkdv_kernel": "bwd.cu", "bwd_dq_kernel": "dq.cu",
            "bwd_rowdot_kernel": "bwd.cu"}[name]
     h = hashlib.sha256()
     for f in (src, "ptx.cuh"):

@@ -16,9 +16,9 @@
 //      tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
 //      S^T/dP^T are double buffered so the next tile's products overlap the
 //      current elementwise work.
-//   3. bwd_dq_kernel: one CTA per 128-query tile; streams 64-key tiles of K and
-//      V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (bf16) written back, and
-//      dQ += dS K_j accumulated in TMEM.
+//   3. bwd_dq_kernel (dq.cu): two 128-query tiles per CTA; streams 64-key
+//      tiles of K and V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (bf16)
+//      written back, and dQ += dS K_j accumulated in TMEM.
 // Causal: key tiles wholly above the diagonal are skipped, diagonal tiles are
 // masked element by element (key j visible to query i iff j <= i).
 #include "kernels.cuh"
@@ -368,254 +368,6 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   if (warp == 5) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-// ---------------------------------------------------------------- dQ
-template <int D>
-struct DqCfg {
-  static constexpr int BM = 128;  // queries per CTA (TMEM lanes)
-  static constexpr int BN = 64;   // keys per step
-  static constexpr int NCHUNK = D / 64;
-  static constexpr int QCHUNK = BM * 128;
-  static constexpr int KCHUNK = BN * 128;
-  static constexpr int QTILE = NCHUNK * QCHUNK;
-  static constexpr int KTILE = NCHUNK * KCHUNK;
-  static constexpr int STAGES = (D == 64) ? 6 : 4;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + QTILE;
-  static constexpr int OFF_K = OFF_DO + QTILE;
-  static constexpr int OFF_V = OFF_K + STAGES * KTILE;
-  static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
-  // At least 120 KB so that only one CTA (which holds all 512 TMEM columns) fits on an SM.
-  static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
-  static constexpr int THREADS = 192;
-  static constexpr uint32_t TM_DQ = 0, TM_BUF = 128, TM_COLS = 512;  // buffer b: S at +128b, dP at +128b+64
-};
-
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ lse, const float* __restrict__ Dws, __nv_bfloat16* __restrict__ dq,
-                  int N, int BH, int n_qtiles, float scale, float scale_log2, unsigned* err) {
-  using C = DqCfg<D>;
-  using Bars = BwdBars<C::STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  EXATTN_TRACE_INIT();
-
-  // Under the causal mask the last query tiles meet the most keys: run them first.
-  const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int q0 = qt * C::BM;
-  const int nk_total = (N + C::BN - 1) / C::BN;
-  const int nk = CAUSAL ? min(nk_total, (q0 + C::BM - 1) / C::BN + 1) : nk_total;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->kv_full, 1);  // here: Q and dO tiles
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&bars->st_full[s], 1);
-      mbar_init(&bars->st_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 128);
-    }
-    mbar_init(&bars->acc_done, 1);
-    mbar_init(&bars->mma_done, 1);
-    bars->abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(&bars->tmem_base, C::TM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-  const WaitCtl wc{&bars->abort, err};
-
-  if (warp == 4) {
-    if (lane == 0) {
-      const uint64_t pol_keep = l2_policy_evict_last();
-      const uint64_t pol_once = l2_policy_evict_first();
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::QTILE);
-      for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_3d(&tm_q, &bars->kv_full, smem + C::OFF_Q + c * C::QCHUNK, c * 64, q0, bh, pol_once);
-        tma_load_3d(&tm_do, &bars->kv_full, smem + C::OFF_DO + c * C::QCHUNK, c * 64, q0, bh, pol_once);
-      }
-      int issued = 0;
-      for (int it = 0; it < nk; ++it) {
-        const int s = it % C::STAGES;
-        const uint32_t ph = (it / C::STAGES) & 1;
-        if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
-        EXATTN_TRACE_POINT(0, it, 0);
-        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
-        for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_3d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      it * C::BN, bh, pol_keep);
-          tma_load_3d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      it * C::BN, bh, pol_keep);
-        }
-        issued = it + 1;
-      }
-      if (*reinterpret_cast<volatile int*>(&bars->abort)) {
-        mbar_wait_drain(&bars->kv_full, 0, err);
-        for (int it = max(0, issued - C::STAGES); it < issued; ++it)
-          mbar_wait_drain(&bars->st_full[it % C::STAGES], (it / C::STAGES) & 1, err);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 5) {
-    // Whole-warp loop, elected lane issues (see elect_one()).
-    constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);
-    constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
-    const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
-    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
-    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
-    const uint64_t k_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::KCHUNK, 1024);
-    constexpr uint32_t kKTileDesc = C::KTILE >> 4;
-    auto issue_products = [&](int it) {
-      const int s = it % C::STAGES, b = it & 1;
-      const uint64_t ka = k_desc + s * kKTileDesc, va = v_desc + s * kKTileDesc;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qo = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
-        const uint32_t ko = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + C::TM_BUF + b * 128, q_desc + qo, ka + ko, idesc_s, kk > 0);
-        mma_ss(tmem + C::TM_BUF + b * 128 + 64, do_desc + qo, va + ko, idesc_s, kk > 0);
-      }
-    };
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
-    };
-    bool ok = wait_all(&bars->kv_full, 0);
-    if (ok) ok = wait_all(&bars->st_full[0], 0);
-    if (ok) {
-      tc_fence_after();
-      if (elect_one()) {
-        issue_products(0);
-        mma_commit(&bars->s_full[0]);
-      }
-      __syncwarp();
-    }
-    for (int it = 0; ok && it < nk; ++it) {
-      const int s = it % C::STAGES, b = it & 1;
-      if (it + 1 < nk) {
-        const int s1 = (it + 1) % C::STAGES;
-        if (!(ok = wait_all(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1))) break;
-        if (lane == 0) EXATTN_TRACE_POINT(1, it, 0);
-        tc_fence_after();
-        if (elect_one()) {
-          issue_products(it + 1);
-          mma_commit(&bars->s_full[b ^ 1]);
-        }
-        __syncwarp();
-        if (lane == 0) EXATTN_TRACE_POINT(1, it, 1);
-      }
-      if (!(ok = wait_all(&bars->p_full[b], (it >> 1) & 1))) break;
-      if (lane == 0) EXATTN_TRACE_POINT(1, it, 2);
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t ka = k_mn + s * kKTileDesc;
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::TM_DQ, tmem + C::TM_BUF + b * 128 + kk * 8, ka + ((kk * 16 * 128) >> 4), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->st_empty[s]);
-      }
-      __syncwarp();
-      if (lane == 0) EXATTN_TRACE_POINT(1, it, 3);
-    }
-    if (elect_one()) {
-      if (ok) mma_commit(&bars->acc_done);
-      mma_commit(&bars->mma_done);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_wait_drain(&bars->mma_done, 0, err);
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ elementwise (thread = query row)
-    const int row = warp * 32 + lane;
-    const int qrow = q0 + row;
-    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-    const bool valid = qrow < N;
-    const float lse2 = valid ? lse[static_cast<size_t>(bh) * N + qrow] * kLog2e : INFINITY;
-    const float Drow = valid ? Dws[static_cast<size_t>(bh) * N + qrow] : 0.f;
-    const float neg_lse2 = -lse2;
-    bool ok = true;
-    for (int it = 0; ok && it < nk; ++it) {
-      const int b = it & 1;
-      if (!(ok = mbar_wait(&bars->s_full[b], (it >> 1) & 1, wc))) break;
-      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 0);
-      tc_fence_after();
-      const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tb, sr[0]);
-      tmem_ld32(tb + 32, sr[1]);
-      tmem_ld32(tb + 64, dr[0]);
-      tmem_ld32(tb + 96, dr[1]);
-      tmem_wait_ld();
-      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 2);
-      const int kj0 = it * C::BN;
-      const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > q0) || (kj0 + C::BN > N);
-      int lim = N - kj0;
-      if (CAUSAL) lim = min(lim, qrow - kj0 + 1);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = h * 32 + 2 * e + u;
-            float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, neg_lse2));
-            if (need_mask && c >= lim) p = 0.f;
-            dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - Drow);
-          }
-          pk[e] = pack_bf16x2(dsv[0], dsv[1]);
-        }
-        tmem_st16(tb + h * 16, pk);  // dS over S
-      }
-      tmem_wait_st();
-      if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 3);
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[b]);
-    }
-    if (ok) ok = mbar_wait(&bars->acc_done, 0, wc);
-    if (ok) {
-      tc_fence_after();
-      __nv_bfloat16* dst_row = dq + (static_cast<size_t>(bh) * N + qrow) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_bits + C::TM_DQ + c * 32, r);
-        tmem_wait_ld();
-        if (valid) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, C::TM_COLS);
-}
-
 // ---------------------------------------------------------------- launch
 template <int D>
 static cudaError_t launch_prep_t(const BwdArgs& a, cudaStream_t stream) {
@@ -641,19 +393,6 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
-static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
-  using C = DqCfg<D>;
-  auto kern = bwd_dq_kernel<D, CAUSAL>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
-  if (e != cudaSuccess) return e;
-  const int n_qt = (a.N + C::BM - 1) / C::BM;
-  kern<<<static_cast<unsigned>(static_cast<long long>(n_qt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.N, a.BH,
-      n_qt, a.scale, a.scale_log2, a.err);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
   return a.d == 64 ? launch_prep_t<64>(a, stream) : launch_prep_t<128>(a, stream);
 }
@@ -661,11 +400,6 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
   if (a.d == 64) return a.causal ? launch_dkdv_t<64, true>(a, stream) : launch_dkdv_t<64, false>(a, stream);
   return a.causal ? launch_dkdv_t<128, true>(a, stream) : launch_dkdv_t<128, false>(a, stream);
-}
-
-cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_dq_t<64, true>(a, stream) : launch_dq_t<64, false>(a, stream);
-  return a.causal ? launch_dq_t<128, true>(a, stream) : launch_dq_t<128, false>(a, stream);
 }
 
 }  // namespace exattn

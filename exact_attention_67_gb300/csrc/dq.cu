@@ -1,0 +1,364 @@
+// dq.cu -- the dQ part of the attention backward for sm_103a, atomic-free.
+//
+// dQ_i = scale sum_j dS_ij k_j with dS_ij = P_ij (dP_ij - D_i), P_ij =
+// exp(scale q_i.k_j - lse_i) recomputed tile by tile from the stored
+// logsumexp ("Gemini 3 Flash的注意力内核重写：算子融合如何实现亚毫秒级推理",
+// §4 重计算).  Every dQ row is summed by one CTA in a fixed key order, so the
+// result is bit-identical run to run without atomics.
+//
+// GB300 mapping (one CTA per SM, 352 threads), the same ping-pong as the
+// forward kernel:
+//   * the CTA owns two 128-row query tiles of one (batch, head); Q and dO of
+//     both stay in shared memory, 64-key tiles of K and V stream through a
+//     TMA ring that both query tiles share;
+//   * warp 9 + t issues the MMAs of query tile t (warp-uniform loop, elected
+//     lane): per key step, dQ_t += dS_t K_j with dS_t read from TMEM, then
+//     S_t = Q_t K_j+1^T and dP_t = dO_t V_j+1^T into TMEM.  With one issuer
+//     per tile the tensor core always has queued work while the other issuer
+//     waits on its tile's hand-off;
+//   * warps 0-3 / 4-7 turn S_t, dP_t into dS_t (bf16, written over S_t) for
+//     tile 0 / tile 1 (thread = query row); while one warpgroup works, the
+//     tensor core runs the other tile's MMAs, which hides the hand-off
+//     latency between the two roles;
+//   * warp 8 issues the TMA loads.
+// TMEM per tile t (base 256 t): dQ_t [0,128), S_t [128,192), dP_t [192,256).
+// Causal: key tiles above the diagonal are skipped per query tile, diagonal
+// tiles masked per element (key j visible to query i iff j <= i).
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace exattn {
+
+namespace {
+
+constexpr float kLog2eDq = 1.4426950408889634f;
+
+template <int D>
+struct DqCfg {
+  static constexpr int BM = 128;  // queries per tile (TMEM lanes); two tiles per CTA
+  static constexpr int BN = 64;   // keys per step
+  static constexpr int NCHUNK = D / 64;
+  static constexpr int QCHUNK = BM * 128;
+  static constexpr int KCHUNK = BN * 128;
+  static constexpr int QTILE = NCHUNK * QCHUNK;
+  static constexpr int KTILE = NCHUNK * KCHUNK;
+  static constexpr int STAGES = (D == 64) ? 6 : 3;
+  static constexpr int OFF_Q = 0;                      // Q_0, Q_1
+  static constexpr int OFF_DO = OFF_Q + 2 * QTILE;     // dO_0, dO_1
+  static constexpr int OFF_K = OFF_DO + 2 * QTILE;
+  static constexpr int OFF_V = OFF_K + STAGES * KTILE;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
+  static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
+  static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit");
+  static constexpr int THREADS = 352;  // warps 0-7 elementwise (two tiles), 8 producer, 9-10 MMA
+  static constexpr uint32_t TM_TILE = 256, TM_DQ = 0, TM_S = 128, TM_DP = 192, TM_COLS = 512;
+};
+
+template <int STAGES>
+struct DqBars {
+  uint64_t qd_full[2];                         // Q_t and dO_t loaded
+  uint64_t st_full[STAGES], st_empty[STAGES];  // K_j, V_j
+  uint64_t s_full[2];                          // S_t, dP_t ready
+  uint64_t p_full[2];                          // dS_t written by the 128 threads of tile t
+  uint64_t acc_done[2];                        // dQ_t final
+  uint64_t turn[2];                            // issuer t may queue its next block of MMAs
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+}  // namespace
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const float* __restrict__ lse, const float* __restrict__ Dws, __nv_bfloat16* __restrict__ dq,
+                  int N, int BH, int n_pairs, float scale, float scale_log2, unsigned* err) {
+  using C = DqCfg<D>;
+  using Bars = DqBars<C::STAGES>;
+  static_assert(sizeof(Bars) <= 512, "barrier block too large");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  EXATTN_TRACE_INIT();
+
+  // Under the causal mask the last query tiles meet the most keys: run them first.
+  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int q0 = pair * 2 * C::BM;
+  const int nk_total = (N + C::BN - 1) / C::BN;
+  // Key steps of query tile t (0 if the tile lies wholly past N).
+  auto steps_for = [&](int t) {
+    const int r0 = q0 + t * C::BM;
+    return (r0 >= N) ? 0 : (CAUSAL ? min(nk_total, (r0 + C::BM - 1) / C::BN + 1) : nk_total);
+  };
+  const int nk0 = steps_for(0), nk1 = steps_for(1);
+  const int n_iter = max(nk0, nk1);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->qd_full[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->acc_done[t], 1);
+      mbar_init(&bars->turn[t], 1);
+    }
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars->st_full[s], 1);
+      mbar_init(&bars->st_empty[s], 2);  // one commit (or arrive) per query tile
+    }
+    mbar_init(&bars->mma_done, 2);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, err};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_keep = l2_policy_evict_last();  // K, V are re-read by every query pair of the head
+      const uint64_t pol_once = l2_policy_evict_first();
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? nk0 : nk1) == 0) continue;
+        mbar_arrive_expect_tx(&bars->qd_full[t], 2 * C::QTILE);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(&tm_q, &bars->qd_full[t], smem + C::OFF_Q + t * C::QTILE + c * C::QCHUNK, c * 64,
+                      q0 + t * C::BM, bh, pol_once);
+          tma_load_3d(&tm_do, &bars->qd_full[t], smem + C::OFF_DO + t * C::QTILE + c * C::QCHUNK, c * 64,
+                      q0 + t * C::BM, bh, pol_once);
+        }
+      }
+      int issued = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (it / C::STAGES) & 1;
+        if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
+        EXATTN_TRACE_POINT(0, it, 0);
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
+                      it * C::BN, bh, pol_keep);
+          tma_load_3d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
+                      it * C::BN, bh, pol_keep);
+        }
+        issued = it + 1;
+      }
+      if (*reinterpret_cast<volatile int*>(&bars->abort)) {
+        // Never leave a copy in flight into shared memory this CTA is about to release.
+        for (int t = 0; t < 2; ++t)
+          if ((t == 0 ? nk0 : nk1) > 0) mbar_wait_drain(&bars->qd_full[t], 0, err);
+        for (int it = max(0, issued - C::STAGES); it < issued; ++it)
+          mbar_wait_drain(&bars->st_full[it % C::STAGES], (it / C::STAGES) & 1, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------ MMA issuers: warp 9 + t drives query tile t
+    // (whole warp, elected lane issues).  Two issuers keep the tensor core fed
+    // while either one waits on its tile's elementwise warps.
+    const int t = warp - 9;
+    const int nk_t = t == 0 ? nk0 : nk1;
+    constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);  // Q (dO) x K^T (V^T): both K-major
+    constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);    // dS from TMEM x K (MN-major)
+    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::KCHUNK, 1024);
+    constexpr uint32_t kQTileDesc = C::QTILE >> 4, kKTileDesc = C::KTILE >> 4;
+
+    auto issue_products = [&](int t, int stage, int kk0, int kk1) {
+      const uint32_t base = tmem + t * C::TM_TILE;
+      const uint64_t qa = q_desc + t * kQTileDesc, da = do_desc + t * kQTileDesc;
+      const uint64_t ka = k_desc + stage * kKTileDesc, va = v_desc + stage * kKTileDesc;
+#pragma unroll
+      for (int kk = kk0; kk < kk1; ++kk) {
+        const uint32_t qo = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
+        const uint32_t ko = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
+        mma_ss(base + C::TM_S, qa + qo, ka + ko, idesc_s, kk > 0);
+        mma_ss(base + C::TM_DP, da + qo, va + ko, idesc_s, kk > 0);
+      }
+    };
+    auto issue_dq = [&](int t, int stage, bool acc) {
+      const uint32_t base = tmem + t * C::TM_TILE;
+      const uint64_t ka = k_mn + stage * kKTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_ts(base + C::TM_DQ, base + C::TM_S + kk * 8, ka + ((kk * 16 * 128) >> 4), idesc_acc,
+               (acc || kk > 0) ? 1u : 0u);
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    };
+
+    bool ok = true;
+    if (nk_t > 0) {
+      ok = wait_all(&bars->qd_full[t], 0) && wait_all(&bars->st_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+          issue_products(t, 0, 0, D / 16);
+          mma_commit(&bars->s_full[t]);
+        }
+        __syncwarp();
+      }
+    }
+    // The two issuers take turns, one block of MMAs (dQ_t, then the next S_t,
+    // dP_t) each.  A block is handed over a few MMAs before its end, so the
+    // next issuer is already queueing while the tensor core finishes it: the
+    // queue in front of the tensor core is shallow, and an empty queue costs
+    // the pipeline's fill latency at every block.
+    constexpr int kTail = D == 128 ? 2 : 1;  // product k-steps left when the turn passes
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t turn_par = static_cast<uint32_t>(it & 1) ^ (t == 0 ? 1u : 0u);
+      if (it >= nk_t) {
+        // No MMA of this tile reads stage s: release it once it holds step it's K, V.
+        if (!(ok = wait_all(&bars->st_full[s], (it / C::STAGES) & 1))) break;
+        if (lane == 0) mbar_arrive(&bars->st_empty[s]);
+        if (!(ok = wait_all(&bars->turn[t], turn_par))) break;
+        if (lane == 0) mbar_arrive(&bars->turn[t ^ 1]);
+        __syncwarp();
+        continue;
+      }
+      const bool more = it + 1 < nk_t;
+      const int s1 = (it + 1) % C::STAGES;
+      if (!(ok = wait_all(&bars->p_full[t], it & 1))) break;
+      if (more && !(ok = wait_all(&bars->st_full[s1], ((it + 1) / C::STAGES) & 1))) break;
+      if (!(ok = wait_all(&bars->turn[t], turn_par))) break;
+      if (lane == 0) EXATTN_TRACE_POINT(1, it, 4 * t + 0);
+      tc_fence_after();
+      if (elect_one()) {
+        issue_dq(t, s, it > 0);
+        mma_commit(&bars->st_empty[s]);  // this tile's last read of K_it, V_it
+        if (more) {
+          // S_t, dP_t of the next step overwrite the dS_t the dQ MMA just read:
+          // the tensor core runs one thread's MMAs in issue order.
+          issue_products(t, s1, 0, D / 16 - kTail);
+          mbar_arrive(&bars->turn[t ^ 1]);
+          issue_products(t, s1, D / 16 - kTail, D / 16);
+          mma_commit(&bars->s_full[t]);
+        } else {
+          mbar_arrive(&bars->turn[t ^ 1]);
+          mma_commit(&bars->acc_done[t]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) EXATTN_TRACE_POINT(1, it, 4 * t + 1);
+    }
+    if (elect_one()) mma_commit(&bars->mma_done);
+    __syncwarp();
+    if (lane == 0) mbar_wait_drain(&bars->mma_done, 0, err);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise (thread = query row of tile t)
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int tile_r0 = q0 + t * C::BM;
+    const int qrow = tile_r0 + row;
+    const int nk_t = t == 0 ? nk0 : nk1;
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tbase = tmem + lane_bits + t * C::TM_TILE;
+    const bool valid = qrow < N;
+    // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
+    const float neg_lse2 = valid ? -lse[static_cast<size_t>(bh) * N + qrow] * kLog2eDq : -INFINITY;
+    const float Drow = valid ? Dws[static_cast<size_t>(bh) * N + qrow] : 0.f;
+    bool ok = nk_t > 0;
+    for (int it = 0; ok && it < nk_t; ++it) {
+      if (!(ok = mbar_wait(&bars->s_full[t], it & 1, wc))) break;
+      if (row == 0) EXATTN_TRACE_POINT(2 + t, it, 0);
+      tc_fence_after();
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(tbase + C::TM_S, sr[0]);
+      tmem_ld32(tbase + C::TM_S + 32, sr[1]);
+      tmem_ld32(tbase + C::TM_DP, dr[0]);
+      tmem_ld32(tbase + C::TM_DP + 32, dr[1]);
+      tmem_wait_ld();
+      const int kj0 = it * C::BN;
+      const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > tile_r0) || (kj0 + C::BN > N);
+      int lim = N - kj0;
+      if (CAUSAL) lim = min(lim, qrow - kj0 + 1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = h * 32 + 2 * e + u;
+            float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, neg_lse2));
+            if (need_mask && c >= lim) p = 0.f;
+            dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - Drow);
+          }
+          pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(tbase + C::TM_S + h * 16, pk);  // dS over the first 32 columns of S
+      }
+      tmem_wait_st();
+      if (lane == 0) EXATTN_TRACE_POINT(2 + t, it, 1 + wq);
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+    }
+    if (ok && nk_t > 0) ok = mbar_wait(&bars->acc_done[t], 0, wc);
+    if (ok && nk_t > 0) {
+      tc_fence_after();
+      __nv_bfloat16* dst_row = dq + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + C::TM_DQ + c * 32, r);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = DqCfg<D>;
+  auto kern = bwd_dq_kernel<D, CAUSAL>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
+  if (e != cudaSuccess) return e;
+  const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
+      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.N, a.BH,
+      n_pairs, a.scale, a.scale_log2, a.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_dq_t<64, true>(a, stream) : launch_dq_t<64, false>(a, stream);
+  return a.causal ? launch_dq_t<128, true>(a, stream) : launch_dq_t<128, false>(a, stream);
+}
+
+}  // namespace exattn
