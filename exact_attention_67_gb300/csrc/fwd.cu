@@ -286,22 +286,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
       const int kv0 = j * C::BN;
       const bool need_mask = (CAUSAL && j == (t == 0 ? nkv0 : nkv1) - 1) || (kv0 + C::BN > N);
-      float mx = -INFINITY;
       if (need_mask) {
         int lim = N - kv0;
         if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < 32; ++e)
             if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, __uint_as_float(sr[c][e]));
-          }
-      } else {
+      }
+      // Row max as eight independent chains of three-input maxima: the
+      // reduction is exact in any order, and a short chain keeps the
+      // warpgroup's latency (which the tensor core waits on) low.
+      float mx;
+      {
+        auto x = [&](int f) { return __uint_as_float(sr[f >> 5][f & 31]); };
+        float pm[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(x(k), x(k + 8));
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        for (int f = 16; f < 128; f += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], x(f + k), x(f + 8 + k));
+        mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       }
       const float m_new = fmaxf(m_ref, mx * scale_log2);
       // Move the reference max only when it grew by more than the threshold.
@@ -318,21 +325,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
       const float neg_m = -m_ref;
-      float rs0 = 0.f, rs1 = 0.f;
+      // Four packed partial sums: short FADD chains, half the instructions.
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), scale_log2, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), scale_log2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          const float2 y = ffma2(make_float2(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])), sc2, nm2);
+          const float2 p = make_float2(ex2(y.x), ex2(y.y));
+          rs[e & 3] = fadd2(rs[e & 3], p);
+          pk[e] = pack_bf16x2(p.x, p.y);
         }
         tmem_st16(tS + c * 16, pk);  // P_t over the first 64 columns of S_t
       }
-      l = l * alpha + (rs0 + rs1);
+      const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+      const float2 r = fadd2(r01, r23);
+      l = l * alpha + (r.x + r.y);
       if (rescale_warp) {
         // S_t(j) ready implies P_t(j-1) V_{j-1} has completed: the O row is stable.
 #pragma unroll
