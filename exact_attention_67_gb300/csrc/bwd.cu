@@ -219,11 +219,11 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     const uint64_t q_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::QCHUNK, 1024);
     const uint64_t do_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::QCHUNK, 1024);
     constexpr uint32_t kQTileDesc = C::QTILE >> 4;
-    auto issue_products = [&](int it) {
+    auto issue_products = [&](int it, int kk0, int kk1) {
       const int s = it % C::STAGES, b = it & 1;
       const uint64_t qa = q_desc + s * kQTileDesc, da = do_desc + s * kQTileDesc;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = kk0; kk < kk1; ++kk) {
         const uint32_t ko = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
         const uint32_t qo = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
         mma_ss(tmem + C::TM_BUF + b * 128, k_desc + ko, qa + qo, idesc_s, kk > 0);
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
-        issue_products(0);
+        issue_products(0, 0, D / 16);
         mma_commit(&bars->s_full[0]);
       }
       __syncwarp();
@@ -251,7 +251,12 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         if (lane == 0) EXATTN_TRACE_POINT(1, it, 0);
         tc_fence_after();
         if (elect_one()) {
-          issue_products(it + 1);
+          // The release of step it-1's Q/dO stage rides inside this block: a
+          // commit between blocks would hold up the next MMA while the
+          // shallow queue in front of the tensor core runs dry.
+          issue_products(it + 1, 0, 1);
+          if (it > 0) mma_commit(&bars->st_empty[(it - 1) % C::STAGES]);
+          issue_products(it + 1, 1, D / 16);
           mma_commit(&bars->s_full[b ^ 1]);
         }
         __syncwarp();
@@ -270,7 +275,10 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
           mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + kk * 8, qa + ((kk * 16 * 128) >> 4), idesc_acc,
                  acc);
         }
-        mma_commit(&bars->st_empty[s]);
+        if (it + 1 == nq) {
+          if (it > 0) mma_commit(&bars->st_empty[(it - 1) % C::STAGES]);
+          mma_commit(&bars->st_empty[s]);
+        }
       }
       __syncwarp();
       if (lane == 0) EXATTN_TRACE_POINT(1, it, 3);

@@ -232,7 +232,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 1);
         tc_fence_after();
-        if (elect_one()) issue_pv(t, s, j > 0);
+        if (elect_one()) {
+          issue_pv(t, s, j > 0);
+          // V_j is free once the last tile's P V_j is done; releasing it here,
+          // inside the block, keeps the block boundary free of commits.
+          if (t == 1 || nkv1 <= j) mma_commit(&bars->v_empty[s]);
+        }
         __syncwarp();
         if (j + 1 < nkv_t) {
           if (!k_ready) {
@@ -252,11 +257,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           __syncwarp();
         }
       }
-      if (elect_one()) {
-        if (v_ready) mma_commit(&bars->v_empty[s]);
-        if (k_ready) mma_commit(&bars->k_empty[s1]);
+      if (k_ready) {
+        if (elect_one()) mma_commit(&bars->k_empty[s1]);
+        __syncwarp();
       }
-      __syncwarp();
     }
     // Nothing may still read shared memory or write TMEM once the CTA tears down.
     if (elect_one()) mma_commit(&bars->mma_done);
