@@ -316,22 +316,32 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       const float* st_D = st_lse2 + C::BR;
       const int qi0 = (i_begin + it) * C::BR;
       const bool need_mask = CAUSAL && (qi0 < k0 + C::BM);
+      // Column statistics come from shared memory as float4 broadcasts: four
+      // columns per load keeps the shared-memory pipe free for the TMA and
+      // TMEM traffic of the other roles.
+      const float4* st_lse4 = reinterpret_cast<const float4*>(st_lse2);
+      const float4* st_D4 = reinterpret_cast<const float4*>(st_D);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[16], dk_[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dsv[2];
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 L4 = st_lse4[h * 8 + q4], D4 = st_D4[h * 8 + q4];
+          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+          float pv[4], dsv[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = h * 32 + 2 * e + u;
-            float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, -st_lse2[c]));
+          for (int w = 0; w < 4; ++w) {
+            const int cl = 4 * q4 + w;  // column within this half
+            const int c = h * 32 + cl;
+            float p = ex2(fmaf(__uint_as_float(sr[h][cl]), scale_log2, -Lv[w]));
             if (need_mask && qi0 + c < key) p = 0.f;
-            pv[u] = p;
-            dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - st_D[c]);
+            pv[w] = p;
+            dsv[w] = p * (__uint_as_float(dr[h][cl]) - Dv[w]);
           }
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
-          dk_[e] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+          pk[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk_[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+          dk_[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
         tmem_st16(tb + h * 16, pk);         // P^T over S^T
         tmem_st16(tb + 64 + h * 16, dk_);   // dS^T over dP^T
