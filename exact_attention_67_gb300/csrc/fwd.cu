@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t tS = tmem + lane_bits + C::TM_S + t * 128;
     const uint32_t tO = tmem + lane_bits + C::TM_O + t * 128;
     float m_ref = -INFINITY;  // reference max, log2 units of the scaled logits
-    float l = 0.f;            // running sum of 2^(x - m_ref)
+    float l = 0.f;            // running sum of 2^(x - m_ref), fp32 terms (for lse)
+    float lb = 0.f;           // the same sum over the bf16-rounded terms the PV MMA uses (for O)
     bool ok = (t == 0 ? nkv0 : nkv1) > 0;
     for (int j = 0; ok && j < (t == 0 ? nkv0 : nkv1); ++j) {
       if (!(ok = mbar_wait(&bars->s_full[t], j & 1, wc))) break;
@@ -329,23 +330,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
       const float neg_m = -m_ref;
-      // Four packed partial sums: short FADD chains, half the instructions.
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // Packed partial sums: short FADD chains, half the instructions.
+      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
+      uint32_t pk[4][16];  // P as bf16 pairs, kept for the rounded sum below
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float2 y = ffma2(make_float2(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])), sc2, nm2);
           const float2 p = make_float2(ex2(y.x), ex2(y.y));
-          rs[e & 3] = fadd2(rs[e & 3], p);
-          pk[e] = pack_bf16x2(p.x, p.y);
+          rs[e & 1] = fadd2(rs[e & 1], p);
+          pk[c][e] = pack_bf16x2(p.x, p.y);
         }
-        tmem_st16(tS + c * 16, pk);  // P_t over the first 64 columns of S_t
+        tmem_st16(tS + c * 16, pk[c]);  // P_t over the first 64 columns of S_t
       }
-      const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
-      const float2 r = fadd2(r01, r23);
+      const float2 r = fadd2(rs[0], rs[1]);
       l = l * alpha + (r.x + r.y);
       if (rescale_warp) {
         // S_t(j) ready implies P_t(j-1) V_{j-1} has completed: the O row is stable.
@@ -363,12 +363,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tc_fence_before();
       if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 1);
       mbar_arrive(&bars->p_full[t]);
+      // O is normalised by the sum of the bf16-rounded weights the PV MMA
+      // used: a row dominated by a few keys then keeps an exact convex
+      // combination of V rows instead of inheriting their rounding.  Done
+      // after the hand-off, off the tensor core's critical path.
+      float2 rb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rb[e & 1] = add_bf16x2_f32x2(pk[c][e], rb[e & 1]);
+      const float2 rbs = fadd2(rb[0], rb[1]);
+      lb = lb * alpha + (rbs.x + rbs.y);
     }
     // ---------------------------------------------------------- epilogue
     if (ok && (t == 0 ? nkv0 : nkv1) > 0) ok = mbar_wait(&bars->o_full[t], 0, wc);
     if (ok && (t == 0 ? nkv0 : nkv1) > 0) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lb;
       __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * N + row_g) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

@@ -326,6 +326,17 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+// c + the two bf16 halves of `pk` (low half to .x), each converted exactly
+// and added in fp32 round-to-nearest (mixed-precision add, sm_100+).
+__device__ __forceinline__ float2 add_bf16x2_f32x2(uint32_t pk, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(pk), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

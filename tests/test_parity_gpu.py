@@ -96,6 +96,19 @@ def test_workload_sampled_parity(orc, cfg):
     print("\n".join(msgs))
 
 
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_workload_full_forward(orc, cfg):
+    """Every element of O and lse at the full workload size against the oracle's
+    full forward (a few seconds to ~15 s of host time per workload).  The widest
+    logits (workload 5, sigma 2) make rows dominated by a handful of keys, the
+    case where the bf16 rounding of P shows most."""
+    w = WORKLOADS[cfg]
+    q, k, v = make_inputs(w)[:3]
+    res = run_gpu(q, k, v, None, w.causal, w.scale, bwd=False)
+    o_ref, lse_ref = orc.attention_fwd(to_f64(q), to_f64(k), to_f64(v), w.causal, w.scale)
+    print(check_fwd(to_f64(res["o"]), res["lse"].double().numpy(), o_ref, lse_ref, f"{w.name} full"))
+
+
 def test_backward_is_deterministic():
     import exact_attention_67_gb300 as ex
     w = WORKLOADS[2]
