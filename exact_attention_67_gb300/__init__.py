@@ -11,32 +11,41 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (EXPORTS, ExattnError, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_preprocess,
-                   attn_bwd_workspace_size, attn_fwd, device_error, library_path, load, status_string, version)
+from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
+                   attn_bwd_preprocess, attn_bwd_workspace_size, attn_fwd, attn_fwd_ex, device_error, library_path,
+                   load, status_string, version)
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "forward", "backward", "device_error", "status_string", "version", "load",
-           "library_path", "ExattnError", "EXPORTS"]
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "Strides", "forward", "backward", "device_error",
+           "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
 
 
 def _default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
+def _plain(*ts) -> bool:
+    import torch
+    return all(t.dtype == torch.bfloat16 and t.is_contiguous() for t in ts)
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """Allocate O (bf16) and lse (fp32) with torch and run ``attn_fwd``."""
+    """Allocate O (same type and memory layout as q) and lse (fp32) with torch
+    and run ``attn_fwd`` (contiguous bf16) or ``attn_fwd_ex`` (f16 or strided
+    [B, H, N, d] views, e.g. ``x.transpose(1, 2)`` of a [B, N, H, d] tensor)."""
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, causal, s, stream)
+    (attn_fwd if _plain(q, k, v, o) else attn_fwd_ex)(q, k, v, o, lse, causal, s, stream)
     return o, lse
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, stream=None,
              workspace=None):
-    """Allocate dQ, dK, dV (and the workspace unless given) and run ``attn_bwd``."""
+    """Allocate dQ, dK, dV (like q, k, v) and the workspace unless given, and run
+    ``attn_bwd`` (contiguous bf16) or ``attn_bwd_ex``."""
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
@@ -44,5 +53,6 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     if workspace is None:
         nbytes = attn_bwd_workspace_size(B, H, N, d, causal)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
+    fn = attn_bwd if _plain(q, k, v, o, dO, dq, dk, dv) else attn_bwd_ex
+    fn(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
     return dq, dk, dv

@@ -23,8 +23,17 @@ STATUS_NAMES = {
 }
 # Every entry point include/exattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_bwd_noalloc", "exattn_status_string", "exattn_device_error",
-           "exattn_watchdog_selftest", "exattn_version")
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_bwd_noalloc", "exattn_status_string",
+           "exattn_device_error", "exattn_watchdog_selftest", "exattn_version")
+
+EXATTN_DTYPE_BF16 = 0
+EXATTN_DTYPE_F16 = 1
+
+
+class Strides(ctypes.Structure):
+    """C ``exattn_strides``: element strides of a [B, H, N, d] view (d contiguous)."""
+    _fields_ = [("b_stride", ctypes.c_longlong), ("h_stride", ctypes.c_longlong),
+                ("n_stride", ctypes.c_longlong)]
 
 
 class ExattnError(RuntimeError):
@@ -62,6 +71,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_dkdv.restype = i
         lib.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_dq.restype = i
+        S = Strides
+        lib.attn_fwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, i, i, i, i, i, f, vp]
+        lib.attn_fwd_ex.restype = i
+        lib.attn_bwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, i, i, i, i, i, f,
+                                    vp, sz, vp]
+        lib.attn_bwd_ex.restype = i
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_noalloc.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
@@ -113,6 +128,55 @@ def _shape4(t: torch.Tensor, name: str):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     return tuple(t.shape)
+
+
+_DTYPES = {torch.bfloat16: EXATTN_DTYPE_BF16, torch.float16: EXATTN_DTYPE_F16}
+
+
+def _view4(t: torch.Tensor, name: str):
+    """Shape, element type code and C strides of a [B, H, N, d] view whose d
+    axis is contiguous (any b, h, n strides the library accepts)."""
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be a [B, H, N, d] view, got {tuple(t.shape)}")
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"{name} must be bfloat16 or float16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.shape[3] > 1 and t.stride(3) != 1:
+        raise ValueError(f"{name}: the d axis must be contiguous (stride 1), got stride {t.stride(3)}")
+    return tuple(t.shape), _DTYPES[t.dtype], Strides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def attn_fwd_ex(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """C ``attn_fwd_ex``: q, k, v, o are [B, H, N, d] views (d contiguous) of one
+    type, bf16 or f16 (a [B, N, H, d] tensor passes as ``x.transpose(1, 2)``);
+    lse fp32 contiguous [B, H, N]."""
+    (B, H, N, d), dt, sq = _view4(q, "q")
+    views = [_view4(t, n) for n, t in (("k", k), ("v", v), ("o", o))]
+    for n, (shape, dtn, _) in zip(("k", "v", "o"), views):
+        if shape != (B, H, N, d) or dtn != dt:
+            raise ValueError(f"{n} shape/dtype differs from q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    _check(load().attn_fwd_ex(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o), views[2][2],
+                              _ptr(lse), B, H, N, d, int(bool(causal)), float(scale), _stream(stream)))
+
+
+def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """C ``attn_bwd_ex`` on [B, H, N, d] views of one 16-bit type."""
+    (B, H, N, d), dt, sq = _view4(q, "q")
+    names = ("k", "v", "o", "dO", "dq", "dk", "dv")
+    views = [_view4(t, n) for n, t in zip(names, (k, v, o, dO, dq, dk, dv))]
+    for n, (shape, dtn, _) in zip(names, views):
+        if shape != (B, H, N, d) or dtn != dt:
+            raise ValueError(f"{n} shape/dtype differs from q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    s = [vw[2] for vw in views]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().attn_bwd_ex(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
+                              _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], B, H, N, d,
+                              int(bool(causal)), float(scale), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

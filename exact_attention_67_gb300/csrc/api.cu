@@ -98,14 +98,21 @@ int device_setup(int* dev_out, unsigned** err_out) {
   return st.status;
 }
 
-// [B*H, N, d] bf16, d contiguous; box = 64 columns (128 bytes) x box_rows rows x 1.
-bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int box_rows) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+// A [B, H, N, d] view (d contiguous, element strides s) as a 4-D map
+// (d, N, H, B); box = 64 columns (128 bytes) x box_rows rows x 1 x 1.
+bool make_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int N, int d, const Strides& s,
+              int box_rows) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+  // A stride along an extent-1 axis is never used; give the encoder a legal one.
+  const long long sn = N > 1 ? s.n : d, sh = H > 1 ? s.h : d, sb = B > 1 ? s.b : d;
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * 2, static_cast<cuuint64_t>(sh) * 2,
+                                 static_cast<cuuint64_t>(sb) * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty = dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return g_encode(m, ty, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -115,6 +122,24 @@ int check_common(int B, int H, int N, int d, float scale) {
   if (static_cast<long long>(B) * H >= (1ll << 24)) return EXATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return EXATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return EXATTN_ERR_VALUE;
+  return EXATTN_OK;
+}
+
+Strides contiguous(int H, int N, int d) {
+  return Strides{static_cast<long long>(H) * N * d, static_cast<long long>(N) * d, static_cast<long long>(d)};
+}
+
+Strides to_strides(const exattn_strides& s) { return Strides{s.b_stride, s.h_stride, s.n_stride}; }
+
+// Strides in elements: non-negative, multiples of 8 (16 bytes, the TMA rule),
+// below 2^36; positive along every axis of extent > 1.
+int check_strides(const exattn_strides& s, int B, int H, int N) {
+  const long long v[3] = {s.b_stride, s.h_stride, s.n_stride};
+  const int ext[3] = {B, H, N};
+  for (int i = 0; i < 3; ++i) {
+    if (v[i] < 0 || v[i] >= (1ll << 36) || (v[i] & 7) != 0) return EXATTN_ERR_ALIGN;
+    if (ext[i] > 1 && v[i] == 0) return EXATTN_ERR_SHAPE;
+  }
   return EXATTN_OK;
 }
 
@@ -134,6 +159,40 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device) {
 
 using namespace exattn;
 
+namespace {
+
+int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const Strides& sk, const void* v,
+             const Strides& sv, void* o, const Strides& so, float* lse, int B, int H, int N, int d, int causal,
+             float scale, void* stream) {
+  int dev = 0;
+  unsigned* err = nullptr;
+  int rc = device_setup(&dev, &err);
+  if (rc != EXATTN_OK) return rc;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, dtype, B, H, N, d, sq, 128) || !make_map(&mk, k, dtype, B, H, N, d, sk, 128) ||
+      !make_map(&mv, v, dtype, B, H, N, d, sv, 128))
+    return EXATTN_ERR_CUDA;
+  FwdArgs a;
+  a.tm_q = &mq;
+  a.tm_k = &mk;
+  a.tm_v = &mv;
+  a.o = o;
+  a.so = so;
+  a.lse = lse;
+  a.N = N;
+  a.H = H;
+  a.BH = B * H;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.dtype = dtype;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.err = err;
+  a.device = dev;
+  return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                         int causal, float scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return EXATTN_ERR_NULL;
@@ -141,27 +200,24 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   if (rc != EXATTN_OK) return rc;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return EXATTN_ERR_ALIGN;
-  int dev = 0;
-  unsigned* err = nullptr;
-  if ((rc = device_setup(&dev, &err)) != EXATTN_OK) return rc;
-  const int BH = B * H;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, BH, N, d, 128) || !make_map(&mk, k, BH, N, d, 128) || !make_map(&mv, v, BH, N, d, 128))
-    return EXATTN_ERR_CUDA;
-  FwdArgs a;
-  a.tm_q = &mq;
-  a.tm_k = &mk;
-  a.tm_v = &mv;
-  a.o = o;
-  a.lse = lse;
-  a.N = N;
-  a.BH = BH;
-  a.d = d;
-  a.causal = causal ? 1 : 0;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  a.err = err;
-  a.device = dev;
-  return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+  const Strides c = contiguous(H, N, d);
+  return fwd_impl(kBF16, q, c, k, c, v, c, o, c, lse, B, H, N, d, causal, scale, stream);
+}
+
+extern "C" int attn_fwd_ex(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                           const void* v, exattn_strides sv, void* o, exattn_strides so, float* lse, int B, int H,
+                           int N, int d, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  const exattn_strides* all[4] = {&sq, &sk, &sv, &so};
+  for (const exattn_strides* s : all)
+    if ((rc = check_strides(*s, B, H, N)) != EXATTN_OK) return rc;
+  return fwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, q, to_strides(sq), k, to_strides(sk), v, to_strides(sv),
+                  o, to_strides(so), lse, B, H, N, d, causal, scale, stream);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d, int causal) {
@@ -180,17 +236,21 @@ struct BwdMaps {
   CUtensorMap m[8];
 };
 
-int bwd_setup(BwdArgs& a, BwdMaps& maps, const void* q, const void* k, const void* v, const void* dO, int B, int H,
-              int N, int d, int causal, float scale) {
+struct BwdInputs {
+  const void* p[4];  // q, k, v, dO (any may be null)
+  Strides s[4];
+};
+
+int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, int H, int N, int d, int causal,
+              float scale) {
   int dev = 0;
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
   if (rc != EXATTN_OK) return rc;
-  const int BH = B * H;
-  const void* src[4] = {q, k, v, dO};
   for (int i = 0; i < 4; ++i) {
-    if (!src[i]) continue;
-    if (!make_map(&maps.m[i], src[i], BH, N, d, 128) || !make_map(&maps.m[4 + i], src[i], BH, N, d, 64))
+    if (!in.p[i]) continue;
+    if (!make_map(&maps.m[i], in.p[i], dtype, B, H, N, d, in.s[i], 128) ||
+        !make_map(&maps.m[4 + i], in.p[i], dtype, B, H, N, d, in.s[i], 64))
       return EXATTN_ERR_CUDA;
   }
   a.tm_q128 = &maps.m[0];
@@ -202,13 +262,47 @@ int bwd_setup(BwdArgs& a, BwdMaps& maps, const void* q, const void* k, const voi
   a.tm_v64 = &maps.m[6];
   a.tm_do64 = &maps.m[7];
   a.N = N;
-  a.BH = BH;
+  a.H = H;
+  a.BH = B * H;
   a.d = d;
   a.causal = causal ? 1 : 0;
+  a.dtype = dtype;
   a.scale = scale;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.err = err;
   a.device = dev;
+  return EXATTN_OK;
+}
+
+BwdInputs contiguous_inputs(const void* q, const void* k, const void* v, const void* dO, int H, int N, int d) {
+  const Strides c = contiguous(H, N, d);
+  return BwdInputs{{q, k, v, dO}, {c, c, c, c}};
+}
+
+// The whole backward: D_i, then dK/dV, then dQ, on one stream.
+int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, const Strides& sdo, const float* lse,
+             void* dq, const Strides& sdq, void* dk, const Strides& sdk, void* dv, const Strides& sdv, int B, int H,
+             int N, int d, int causal, float scale, void* workspace, void* stream) {
+  BwdArgs a{};
+  BwdMaps maps;
+  int rc = bwd_setup(a, maps, dtype, in, B, H, N, d, causal, scale);
+  if (rc != EXATTN_OK) return rc;
+  a.o = o;
+  a.so = so;
+  a.dO = in.p[3];
+  a.sdo = sdo;
+  a.lse = lse;
+  a.dq = dq;
+  a.sdq = sdq;
+  a.dk = dk;
+  a.sdk = sdk;
+  a.dv = dv;
+  a.sdv = sdv;
+  a.D = static_cast<float*>(workspace);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_bwd_prep(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (launch_bwd_dkdv(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (launch_bwd_dq(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
 
@@ -222,9 +316,12 @@ extern "C" int attn_bwd_preprocess(const void* o, const void* dO, float* D, int 
   if (!aligned(o, 16) || !aligned(dO, 16) || !aligned(D, 4)) return EXATTN_ERR_ALIGN;
   BwdArgs a{};
   BwdMaps maps;
-  if ((rc = bwd_setup(a, maps, nullptr, nullptr, nullptr, nullptr, B, H, N, d, 0, 1.f)) != EXATTN_OK) return rc;
+  const BwdInputs none = contiguous_inputs(nullptr, nullptr, nullptr, nullptr, H, N, d);
+  if ((rc = bwd_setup(a, maps, kBF16, none, B, H, N, d, 0, 1.f)) != EXATTN_OK) return rc;
   a.o = o;
+  a.so = contiguous(H, N, d);
   a.dO = dO;
+  a.sdo = a.so;
   a.D = D;
   return launch_bwd_prep(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
@@ -240,11 +337,15 @@ extern "C" int attn_bwd_dkdv(const void* q, const void* k, const void* v, const 
     return EXATTN_ERR_ALIGN;
   BwdArgs a{};
   BwdMaps maps;
-  if ((rc = bwd_setup(a, maps, q, k, v, dO, B, H, N, d, causal, scale)) != EXATTN_OK) return rc;
+  if ((rc = bwd_setup(a, maps, kBF16, contiguous_inputs(q, k, v, dO, H, N, d), B, H, N, d, causal, scale)) !=
+      EXATTN_OK)
+    return rc;
   a.lse = lse;
   a.D = const_cast<float*>(D);
   a.dk = dk;
+  a.sdk = contiguous(H, N, d);
   a.dv = dv;
+  a.sdv = a.sdk;
   return launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
@@ -259,10 +360,13 @@ extern "C" int attn_bwd_dq(const void* q, const void* k, const void* v, const vo
     return EXATTN_ERR_ALIGN;
   BwdArgs a{};
   BwdMaps maps;
-  if ((rc = bwd_setup(a, maps, q, k, v, dO, B, H, N, d, causal, scale)) != EXATTN_OK) return rc;
+  if ((rc = bwd_setup(a, maps, kBF16, contiguous_inputs(q, k, v, dO, H, N, d), B, H, N, d, causal, scale)) !=
+      EXATTN_OK)
+    return rc;
   a.lse = lse;
   a.D = const_cast<float*>(D);
   a.dq = dq;
+  a.sdq = contiguous(H, N, d);
   return launch_bwd_dq(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
@@ -277,21 +381,32 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     return EXATTN_ERR_ALIGN;
   if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, N, d, causal)) return EXATTN_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
-  BwdArgs a{};
-  BwdMaps maps;
-  if ((rc = bwd_setup(a, maps, q, k, v, dO, B, H, N, d, causal, scale)) != EXATTN_OK) return rc;
-  a.o = o;
-  a.dO = dO;
-  a.lse = lse;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.D = static_cast<float*>(workspace);
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_bwd_prep(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
-  if (launch_bwd_dkdv(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
-  if (launch_bwd_dq(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
-  return EXATTN_OK;
+  const Strides c = contiguous(H, N, d);
+  return bwd_impl(kBF16, contiguous_inputs(q, k, v, dO, H, N, d), o, c, c, lse, dq, c, dk, c, dv, c, B, H, N, d,
+                  causal, scale, workspace, stream);
+}
+
+extern "C" int attn_bwd_ex(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                           const void* v, exattn_strides sv, const void* o, exattn_strides so, const void* dO,
+                           exattn_strides sdo, const float* lse, void* dq, exattn_strides sdq, void* dk,
+                           exattn_strides sdk, void* dv, exattn_strides sdv, int B, int H, int N, int d, int causal,
+                           float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  const exattn_strides* all[8] = {&sq, &sk, &sv, &so, &sdo, &sdq, &sdk, &sdv};
+  for (const exattn_strides* s : all)
+    if ((rc = check_strides(*s, B, H, N)) != EXATTN_OK) return rc;
+  if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, N, d, causal)) return EXATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
+  const BwdInputs in{{q, k, v, dO}, {to_strides(sq), to_strides(sk), to_strides(sv), to_strides(sdo)}};
+  return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, o, to_strides(so), to_strides(sdo), lse, dq,
+                  to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, N, d, causal, scale, workspace,
+                  stream);
 }
 
 extern "C" const char* exattn_status_string(int status) {

@@ -12,13 +12,13 @@
 //   2. bwd_dkdv_kernel: one CTA per 128-key tile; streams 64-query tiles of
 //      Q and dO (TMA ring); per tile the tensor core computes S^T = K Q_i^T
 //      and dP^T = V dO_i^T into TMEM, a warpgroup (thread = key row) turns them
-//      into P^T and dS^T (bf16, written back over S^T and dP^T), and the
+//      into P^T and dS^T (input type, written back over S^T and dP^T), and the
 //      tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
 //      S^T/dP^T are double buffered so the next tile's products overlap the
 //      current elementwise work.
 //   3. bwd_dq_kernel (dq.cu): two 128-query tiles per CTA; streams 64-key
-//      tiles of K and V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (bf16)
-//      written back, and dQ += dS K_j accumulated in TMEM.
+//      tiles of K and V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (input
+//      type) written back, and dQ += dS K_j accumulated in TMEM.
 // Causal: key tiles wholly above the diagonal are skipped, diagonal tiles are
 // masked element by element (key j visible to query i iff j <= i).
 #include "kernels.cuh"
@@ -29,30 +29,32 @@ namespace exattn {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- D_i
-template <int D>
-__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
-                                                         const __nv_bfloat16* __restrict__ dO,
-                                                         float* __restrict__ Dout, long long rows) {
-  constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o, Strides so,
+                                                         const T* __restrict__ dO, Strides sdo,
+                                                         float* __restrict__ Dout, long long rows, int N, int H) {
+  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
   constexpr int RPW = 32 / TPR;
   const int lane = threadIdx.x & 31;
   const long long warp_g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int sub = lane / TPR, part = lane % TPR;
   for (long long r0 = warp_g * RPW; r0 < rows; r0 += n_warps * RPW) {
-    const long long r = r0 + sub;
+    const long long r = r0 + sub;  // row of [B*H, N]
     float acc = 0.f;
     if (r < rows) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + r * D) + part);
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + r * D) + part);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+      // B*H*N < 2^31 (checked at the C ABI): 32-bit index arithmetic.
+      const int ri = static_cast<int>(r), bh = ri / N, n = ri - bh * N, b = bh / H, h = bh - b * H;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + b * so.b + h * so.h + n * so.n) + part);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(dO + b * sdo.b + h * sdo.h + n * sdo.n) + part);
+      const uint32_t* a2 = reinterpret_cast<const uint32_t*>(&a);
+      const uint32_t* c2 = reinterpret_cast<const uint32_t*>(&c);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 fa = __bfloat1622float2(a2[e]);
-        const float2 fb = __bfloat1622float2(b2[e]);
-        acc = fmaf(fa.x, fb.x, acc);
-        acc = fmaf(fa.y, fb.y, acc);
+        const float2 fa = Elem<T>::unpack(a2[e]);
+        const float2 fc = Elem<T>::unpack(c2[e]);
+        acc = fmaf(fa.x, fc.x, acc);
+        acc = fmaf(fa.y, fc.y, acc);
       }
     }
 #pragma unroll
@@ -96,14 +98,15 @@ struct BwdBars {
   int abort;
 };
 
-template <int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const float* __restrict__ lse, const float* __restrict__ Dws, __nv_bfloat16* __restrict__ dk,
-                    __nv_bfloat16* __restrict__ dv, int N, int BH, int n_ktiles, float scale, float scale_log2,
-                    unsigned* err) {
+                    const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dk, Strides sdk,
+                    T* __restrict__ dv, Strides sdv, int N, int H, int BH, int n_ktiles, float scale,
+                    float scale_log2, unsigned* err) {
   using C = DkdvCfg<D>;
+  using E = Elem<T>;
   using Bars = BwdBars<C::STAGES>;
   static_assert(sizeof(Bars) <= 512, "barrier block too large");
   extern __shared__ uint8_t smem_raw[];
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   // Under the causal mask the first key tiles meet the most queries: run them first.
   const int kt = static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
   const int k0 = kt * C::BM;
   const int nq_total = (N + C::BR - 1) / C::BR;
   const int i_begin = CAUSAL ? (k0 / C::BR) : 0;
@@ -154,8 +158,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KTILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_3d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, k0, bh, pol_keep);
-        tma_load_3d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, k0, bh, pol_keep);
+        tma_load_4d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, k0, hh, bb, pol_keep);
+        tma_load_4d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, k0, hh, bb, pol_keep);
       }
     }
     // Row terms of the next step are fetched into registers one step ahead, so
@@ -192,9 +196,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_3d(&tm_q, &bars->st_full[s], smem + C::OFF_Q + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, bh,
+          tma_load_4d(&tm_q, &bars->st_full[s], smem + C::OFF_Q + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, hh, bb,
                       pol_keep);
-          tma_load_3d(&tm_do, &bars->st_full[s], smem + C::OFF_DO + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, bh,
+          tma_load_4d(&tm_do, &bars->st_full[s], smem + C::OFF_DO + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, hh, bb,
                       pol_keep);
         }
         EXATTN_TRACE_POINT(0, it, 1);
@@ -210,8 +214,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     // Whole-warp loop, elected lane issues (see elect_one()).
-    constexpr uint32_t idesc_s = idesc_bf16(128, C::BR, 0, 0);  // K (or V) x Q^T (or dO^T): both K-major
-    constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);    // TMEM operand x (Q or dO), MN-major
+    constexpr uint32_t idesc_s = idesc_f16kind(E::kFmt, 128, C::BR, 0, 0);  // K (or V) x Q^T (or dO^T): K-major
+    constexpr uint32_t idesc_acc = idesc_f16kind(E::kFmt, 128, D, 0, 1);    // TMEM operand x (Q or dO), MN-major
     const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
     const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
@@ -338,10 +342,10 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
             pv[w] = p;
             dsv[w] = p * (__uint_as_float(dr[h][cl]) - Dv[w]);
           }
-          pk[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-          pk[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk_[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-          dk_[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          pk[2 * q4] = E::pack(pv[0], pv[1]);
+          pk[2 * q4 + 1] = E::pack(pv[2], pv[3]);
+          dk_[2 * q4] = E::pack(dsv[0], dsv[1]);
+          dk_[2 * q4 + 1] = E::pack(dsv[2], dsv[3]);
         }
         tmem_st16(tb + h * 16, pk);         // P^T over S^T
         tmem_st16(tb + 64 + h * 16, dk_);   // dS^T over dP^T
@@ -354,12 +358,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     if (ok) ok = mbar_wait(&bars->acc_done, 0, wc);
     if (ok) {
       tc_fence_after();
-      const size_t base = (static_cast<size_t>(bh) * N + key) * D;
+
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t tacc = tmem + lane_bits + (which == 0 ? C::TM_DK : C::TM_DV);
         const float mul = which == 0 ? scale : 1.f;
-        __nv_bfloat16* dst_row = (which == 0 ? dk : dv) + base;
+        const Strides& so = which == 0 ? sdk : sdv;
+        T* dst_row = (which == 0 ? dk : dv) + bb * so.b + hh * so.h + static_cast<long long>(key) * so.n;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+              pk[e] = E::pack(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
             uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
@@ -387,37 +392,47 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- launch
-template <int D>
+template <typename T, int D>
 static cudaError_t launch_prep_t(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.BH) * a.N;
   const int rpb = 256 / (D / 8);  // rows per 256-thread block
   long long blocks = (rows + rpb - 1) / rpb;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  bwd_rowdot_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.D, rows);
+  bwd_rowdot_kernel<T, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.D, rows, a.N, a.H);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL>
 static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   using C = DkdvCfg<D>;
-  auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+  auto kern = bwd_dkdv_kernel<T, D, CAUSAL>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
   const int n_kt = (a.N + C::BM - 1) / C::BM;
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
-      static_cast<__nv_bfloat16*>(a.dv), a.N, a.BH, n_kt, a.scale, a.scale_log2, a.err);
+      *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
+      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, a.scale, a.scale_log2, a.err);
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_prep_dt(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_prep_t<T, 64>(a, stream) : launch_prep_t<T, 128>(a, stream);
+}
+
+template <typename T>
+static cudaError_t launch_dkdv_dt(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_dkdv_t<T, 64, true>(a, stream) : launch_dkdv_t<T, 64, false>(a, stream);
+  return a.causal ? launch_dkdv_t<T, 128, true>(a, stream) : launch_dkdv_t<T, 128, false>(a, stream);
+}
+
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_prep_t<64>(a, stream) : launch_prep_t<128>(a, stream);
+  return a.dtype == kF16 ? launch_prep_dt<__half>(a, stream) : launch_prep_dt<__nv_bfloat16>(a, stream);
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_dkdv_t<64, true>(a, stream) : launch_dkdv_t<64, false>(a, stream);
-  return a.causal ? launch_dkdv_t<128, true>(a, stream) : launch_dkdv_t<128, false>(a, stream);
+  return a.dtype == kF16 ? launch_dkdv_dt<__half>(a, stream) : launch_dkdv_dt<__nv_bfloat16>(a, stream);
 }
 
 }  // namespace exattn

@@ -16,7 +16,7 @@
 //     S_t = Q_t K_j+1^T and dP_t = dO_t V_j+1^T into TMEM.  With one issuer
 //     per tile the tensor core always has queued work while the other issuer
 //     waits on its tile's hand-off;
-//   * warps 0-3 / 4-7 turn S_t, dP_t into dS_t (bf16, written over S_t) for
+//   * warps 0-3 / 4-7 turn S_t, dP_t into dS_t (input type, written over S_t) for
 //     tile 0 / tile 1 (thread = query row); while one warpgroup works, the
 //     tensor core runs the other tile's MMAs, which hides the hand-off
 //     latency between the two roles;
@@ -69,13 +69,14 @@ struct DqBars {
 
 }  // namespace
 
-template <int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ lse, const float* __restrict__ Dws, __nv_bfloat16* __restrict__ dq,
-                  int N, int BH, int n_pairs, float scale, float scale_log2, unsigned* err) {
+                  const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dq, Strides sdq,
+                  int N, int H, int BH, int n_pairs, float scale, float scale_log2, unsigned* err) {
   using C = DqCfg<D>;
+  using E = Elem<T>;
   using Bars = DqBars<C::STAGES>;
   static_assert(sizeof(Bars) <= 512, "barrier block too large");
   extern __shared__ uint8_t smem_raw[];
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   // Under the causal mask the last query tiles meet the most keys: run them first.
   const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
   const int q0 = pair * 2 * C::BM;
   const int nk_total = (N + C::BN - 1) / C::BN;
   // Key steps of query tile t (0 if the tile lies wholly past N).
@@ -135,10 +137,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         if ((t == 0 ? nk0 : nk1) == 0) continue;
         mbar_arrive_expect_tx(&bars->qd_full[t], 2 * C::QTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_3d(&tm_q, &bars->qd_full[t], smem + C::OFF_Q + t * C::QTILE + c * C::QCHUNK, c * 64,
-                      q0 + t * C::BM, bh, pol_once);
-          tma_load_3d(&tm_do, &bars->qd_full[t], smem + C::OFF_DO + t * C::QTILE + c * C::QCHUNK, c * 64,
-                      q0 + t * C::BM, bh, pol_once);
+          tma_load_4d(&tm_q, &bars->qd_full[t], smem + C::OFF_Q + t * C::QTILE + c * C::QCHUNK, c * 64,
+                      q0 + t * C::BM, hh, bb, pol_once);
+          tma_load_4d(&tm_do, &bars->qd_full[t], smem + C::OFF_DO + t * C::QTILE + c * C::QCHUNK, c * 64,
+                      q0 + t * C::BM, hh, bb, pol_once);
         }
       }
       int issued = 0;
@@ -149,10 +151,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         EXATTN_TRACE_POINT(0, it, 0);
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_3d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      it * C::BN, bh, pol_keep);
-          tma_load_3d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      it * C::BN, bh, pol_keep);
+          tma_load_4d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
+                      it * C::BN, hh, bb, pol_keep);
+          tma_load_4d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
+                      it * C::BN, hh, bb, pol_keep);
         }
         issued = it + 1;
       }
@@ -171,8 +173,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     // while either one waits on its tile's elementwise warps.
     const int t = warp - 9;
     const int nk_t = t == 0 ? nk0 : nk1;
-    constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);  // Q (dO) x K^T (V^T): both K-major
-    constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);    // dS from TMEM x K (MN-major)
+    constexpr uint32_t idesc_s = idesc_f16kind(E::kFmt, 128, C::BN, 0, 0);  // Q (dO) x K^T (V^T): both K-major
+    constexpr uint32_t idesc_acc = idesc_f16kind(E::kFmt, 128, D, 0, 1);    // dS from TMEM x K (MN-major)
     const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
     const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
     const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             if (need_mask && c >= lim) p = 0.f;
             dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - Drow);
           }
-          pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[e] = E::pack(dsv[0], dsv[1]);
         }
         tmem_st16(tbase + C::TM_S + h * 16, pk);  // dS over the first 32 columns of S
       }
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     if (ok && nk_t > 0) ok = mbar_wait(&bars->acc_done[t], 0, wc);
     if (ok && nk_t > 0) {
       tc_fence_after();
-      __nv_bfloat16* dst_row = dq + (static_cast<size_t>(bh) * N + qrow) * D;
+      T* dst_row = dq + bb * sdq.b + hh * sdq.h + static_cast<long long>(qrow) * sdq.n;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
+            pk[e] = E::pack(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
           uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -343,22 +345,27 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   if (warp == 9) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-template <int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL>
 static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   using C = DqCfg<D>;
-  auto kern = bwd_dq_kernel<D, CAUSAL>;
+  auto kern = bwd_dq_kernel<T, D, CAUSAL>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.N, a.BH,
-      n_pairs, a.scale, a.scale_log2, a.err);
+      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<T*>(a.dq), a.sdq, a.N, a.H,
+      a.BH, n_pairs, a.scale, a.scale_log2, a.err);
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_dq_dt(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_dq_t<T, 64, true>(a, stream) : launch_dq_t<T, 64, false>(a, stream);
+  return a.causal ? launch_dq_t<T, 128, true>(a, stream) : launch_dq_t<T, 128, false>(a, stream);
+}
+
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_dq_t<64, true>(a, stream) : launch_dq_t<64, false>(a, stream);
-  return a.causal ? launch_dq_t<128, true>(a, stream) : launch_dq_t<128, false>(a, stream);
+  return a.dtype == kF16 ? launch_dq_dt<__half>(a, stream) : launch_dq_dt<__nv_bfloat16>(a, stream);
 }
 
 }  // namespace exattn

@@ -21,10 +21,12 @@
 //     128 scores, updates the running max, rescales the running sum and the
 //     TMEM O row when the max has grown by more than 2^8 (the reference max
 //     is otherwise kept; the final normalisation by the same reference makes
-//     the result identical), writes P = 2^(s*scale*log2e - m) as bf16 over
-//     the S columns, and hands the tile back to the MMA warp.  While one
-//     warpgroup does its softmax the tensor core works on the other tile.
-//   * epilogue: O_t / l rounded to bf16 and lse = (m + log2 l) ln 2.
+//     the result identical), writes P = 2^(s*scale*log2e - m) in the input
+//     type (bf16 or f16) over the S columns, and hands the tile back to the
+//     MMA warp.  While one warpgroup does its softmax the tensor core works
+//     on the other tile.
+//   * epilogue: O_t / l rounded to the input type, lse = (m + log2 l) ln 2;
+//     l for O sums the rounded P that the PV MMA used.
 // TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -65,12 +67,14 @@ struct FwdBars {
 // Rescale threshold for the running max, in log2 units: P stays below 2^8.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse_out, int N, int BH, int n_pairs, float scale_log2, unsigned* err) {
+                    const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
+                    float* __restrict__ lse_out, int N, int H, int BH, int n_pairs, float scale_log2,
+                    unsigned* err) {
   using C = FwdCfg<D>;
+  using E = Elem<T>;
   using Bars = FwdBars<C::STAGES>;
   static_assert(sizeof(Bars) <= 512, "barrier block too large");
   extern __shared__ uint8_t smem_raw[];
@@ -82,6 +86,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   // Heaviest work first: under the causal mask the last query pairs see the most keys.
   const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
   const int q0 = pair * 2 * C::BM;
   const int nkv_total = (N + C::BN - 1) / C::BN;
   // Key tiles visited by query tile t (0 if the tile lies wholly past N).
@@ -132,8 +137,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if ((t == 0 ? nkv0 : nkv1) == 0) continue;
         mbar_arrive_expect_tx(&bars->q_full[t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(&tm_q, &bars->q_full[t], smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      q0 + t * C::BM, bh, pol_q);
+          tma_load_4d(&tm_q, &bars->q_full[t], smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
+                      q0 + t * C::BM, hh, bb, pol_q);
       }
       int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_iter; ++j) {
@@ -143,15 +148,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         EXATTN_TRACE_POINT(0, j, 0);
         mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(&tm_k, &bars->k_full[s], smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      j * C::BN, bh, pol_kv);
+          tma_load_4d(&tm_k, &bars->k_full[s], smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
+                      j * C::BN, hh, bb, pol_kv);
         issued_k = j + 1;
         if (!mbar_wait(&bars->v_empty[s], ph ^ 1, wc)) break;
         EXATTN_TRACE_POINT(0, j, 1);
         mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(&tm_v, &bars->v_full[s], smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      j * C::BN, bh, pol_kv);
+          tma_load_4d(&tm_v, &bars->v_full[s], smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
+                      j * C::BN, hh, bb, pol_kv);
         issued_v = j + 1;
       }
       if (*reinterpret_cast<volatile int*>(&bars->abort)) {
@@ -169,8 +174,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (waits and descriptor arithmetic stay
     // warp-uniform); the elected lane issues the tcgen05 instructions.
-    constexpr uint32_t idesc_s = idesc_bf16(128, C::BN, 0, 0);  // Q, K both K-major
-    constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);      // P from TMEM, V MN-major
+    constexpr uint32_t idesc_s = idesc_f16kind(E::kFmt, 128, C::BN, 0, 0);  // Q, K both K-major
+    constexpr uint32_t idesc_o = idesc_f16kind(E::kFmt, 128, D, 0, 1);      // P from TMEM, V MN-major
     const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
     const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::CHUNK_BYTES, 1024);
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const float2 y = ffma2(make_float2(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])), sc2, nm2);
           const float2 p = make_float2(ex2(y.x), ex2(y.y));
           rs[e & 1] = fadd2(rs[e & 1], p);
-          pk[c][e] = pack_bf16x2(p.x, p.y);
+          pk[c][e] = E::pack(p.x, p.y);
         }
         tmem_st16(tS + c * 16, pk[c]);  // P_t over the first 64 columns of S_t
       }
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) rb[e & 1] = add_bf16x2_f32x2(pk[c][e], rb[e & 1]);
+        for (int e = 0; e < 16; ++e) rb[e & 1] = E::add_pair(pk[c][e], rb[e & 1]);
       const float2 rbs = fadd2(rb[0], rb[1]);
       lb = lb * alpha + (rbs.x + rbs.y);
     }
@@ -380,7 +385,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (ok && (t == 0 ? nkv0 : nkv1) > 0) {
       tc_fence_after();
       const float inv_l = 1.f / lb;
-      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * N + row_g) * D;
+      T* orow = out + bb * so.b + hh * so.h + static_cast<long long>(row_g) * so.n;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o_r[32];
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(o_r[2 * e]) * inv_l, __uint_as_float(o_r[2 * e + 1]) * inv_l);
+            pk[e] = E::pack(__uint_as_float(o_r[2 * e]) * inv_l, __uint_as_float(o_r[2 * e + 1]) * inv_l);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -407,22 +412,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (warp == 9) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-template <int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL>
 static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  auto kern = attn_fwd_kernel<T, D, CAUSAL>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long grid = static_cast<long long>(n_pairs) * a.BH;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.N, a.BH, n_pairs, a.scale_log2, a.err);
+      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, a.scale_log2,
+      a.err);
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_fwd_dt(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_fwd_t<T, 64, true>(a, stream) : launch_fwd_t<T, 64, false>(a, stream);
+  return a.causal ? launch_fwd_t<T, 128, true>(a, stream) : launch_fwd_t<T, 128, false>(a, stream);
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
-  return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+  return a.dtype == kF16 ? launch_fwd_dt<__half>(a, stream) : launch_fwd_dt<__nv_bfloat16>(a, stream);
 }
 
 }  // namespace exattn

@@ -6,40 +6,51 @@
 
 namespace exattn {
 
+// Element strides of a [B, H, N, d] view whose d axis is contiguous.
+struct Strides {
+  long long b, h, n;
+};
+
+// Element type of Q, K, V, O, dO, dQ, dK, dV (the C ABI's exattn_dtype).
+enum : int { kBF16 = 0, kF16 = 1 };
+
 struct FwdArgs {
-  const CUtensorMap* tm_q;  // 3-D maps over [B*H, N, d] bf16, box 64 x 128 x 1, 128-byte swizzle
+  const CUtensorMap* tm_q;  // 4-D maps (d, N, H, B), box 64 x 128 x 1 x 1, 128-byte swizzle
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
-  void* o;                  // bf16 [B*H, N, d]
+  void* o;                  // [B, H, N, d] view with strides so
+  Strides so;
   float* lse;               // fp32 [B*H, N]
-  int N, BH, d, causal;
+  int N, H, BH, d, causal, dtype;
   float scale_log2;         // scale * log2(e)
   unsigned* err;            // device watchdog word
   int device;
 };
 
 struct BwdArgs {
-  // 3-D maps over [B*H, N, d] bf16 with 128-byte swizzle; box 64 x 128 x 1 ...
+  // 4-D maps (d, N, H, B) with 128-byte swizzle; box 64 x 128 x 1 x 1 ...
   const CUtensorMap* tm_q128;
   const CUtensorMap* tm_k128;
   const CUtensorMap* tm_v128;
   const CUtensorMap* tm_do128;
-  // ... and box 64 x 64 x 1
+  // ... and box 64 x 64 x 1 x 1
   const CUtensorMap* tm_q64;
   const CUtensorMap* tm_k64;
   const CUtensorMap* tm_v64;
   const CUtensorMap* tm_do64;
-  const void* q;            // raw pointers, bf16 [B*H, N, d]
-  const void* k;
-  const void* v;
-  const void* o;
+  const void* o;            // [B, H, N, d] views (d contiguous) with their element strides
+  Strides so;
   const void* dO;
-  const float* lse;         // fp32 [B*H, N], natural log
+  Strides sdo;
   void* dq;
+  Strides sdq;
   void* dk;
+  Strides sdk;
   void* dv;
+  Strides sdv;
+  const float* lse;         // fp32 [B*H, N], natural log
   float* D;                 // workspace: fp32 [B*H, N]
-  int N, BH, d, causal;
+  int N, H, BH, d, causal, dtype;
   float scale, scale_log2;
   unsigned* err;
   int device;

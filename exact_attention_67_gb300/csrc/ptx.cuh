@@ -8,6 +8,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace exattn {
@@ -159,6 +160,17 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* m, uint64_t* bar,
       : "memory");
 }
 
+// 4-D tiled load: coordinates (c0 innermost) of a map over a [B, H, N, d]
+// view with arbitrary b, h, n strides.
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* m, uint64_t* bar, void* dst, int c0, int c1,
+                                            int c2, int c3, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(cache_hint)
+      : "memory");
+}
+
 // L2 eviction-priority policies for the cache_hint operand.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
@@ -220,12 +232,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
+// Instruction descriptor, kind::f16 with fp32 D; A and B share one format
+// (0 = f16, 1 = bf16).
+//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format,
 //   15 A major (0 = K-major, 1 = MN-major), 16 B major, 17-22 N>>3, 24-28 M>>4.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int ab_fmt, int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (uint32_t(ab_fmt) << 7) | (uint32_t(ab_fmt) << 10) | (uint32_t(a_mn_major) << 15) |
+         (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
-         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+  return idesc_f16kind(1, M, N, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -341,6 +357,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// c + the two f16 halves of `pk` (low half to .x), as add_bf16x2_f32x2.
+__device__ __forceinline__ float2 add_f16x2_f32x2(uint32_t pk, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(pk), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// The two 16-bit input types of the kind::f16 MMA: format code, RNE packing
+// of fp32 pairs, exact widening of packed pairs.
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kFmt = 1;
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  __device__ static __forceinline__ float2 add_pair(uint32_t pk, float2 c) { return add_bf16x2_f32x2(pk, c); }
+  __device__ static __forceinline__ float2 unpack(uint32_t pk) {
+    return make_float2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u));
+  }
+};
+template <>
+struct Elem<__half> {
+  static constexpr int kFmt = 0;
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
+  __device__ static __forceinline__ float2 add_pair(uint32_t pk, float2 c) { return add_f16x2_f32x2(pk, c); }
+  __device__ static __forceinline__ float2 unpack(uint32_t pk) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&pk));
+  }
+};
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -60,14 +60,14 @@ WORKLOADS = {
 }
 
 
-def seeded_bf16(shape, seed: int, sigma: float = 1.0) -> torch.Tensor:
+def seeded_bf16(shape, seed: int, sigma: float = 1.0, dtype=torch.bfloat16) -> torch.Tensor:
     """fp32 N(0, 1) from a CPU generator seeded with ``seed``, times sigma,
-    rounded to bf16."""
+    rounded to ``dtype`` (bf16 unless asked for f16)."""
     g = torch.Generator().manual_seed(int(seed))
     x = torch.randn(*shape, generator=g, dtype=torch.float32)
     if sigma != 1.0:
         x = x * sigma
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
 def make_inputs(w: Workload, seed_base: int | None = None, with_grad: bool | None = None):
@@ -85,7 +85,10 @@ def make_inputs(w: Workload, seed_base: int | None = None, with_grad: bool | Non
     return q, k, v
 
 
-def custom(B: int, H: int, N: int, d: int, causal: bool, seed: int, sigma_qk: float = 1.0):
-    """Inputs for an ad-hoc shape (edge-case tests): Q, K, V, dO, bf16 CPU."""
+def custom(B: int, H: int, N: int, d: int, causal: bool, seed: int, sigma_qk: float = 1.0, dtype=torch.bfloat16):
+    """Inputs for an ad-hoc shape (edge-case tests): Q, K, V, dO on the CPU,
+    contiguous [B, H, N, d], bf16 (or f16)."""
     w = Workload(0, B, H, N, d, causal, True, sigma_qk)
-    return w, make_inputs(w, seed_base=seed, with_grad=True)
+    shape = (B, H, N, d)
+    ins = tuple(seeded_bf16(shape, seed + t, sigma_qk if t < 2 else 1.0, dtype) for t in range(4))
+    return w, ins

@@ -126,6 +126,53 @@ int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, con
                 void* dq, int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
+ * Element type and layout for the _ex calls below.  The flash_attn_func
+ * example of "提示词再优也救不了的性能黑洞…", 第一章, passes fp16 tensors laid
+ * out [batch, seqlen, heads, head_dim]; the _ex calls accept that layout (or
+ * any other whose head_dim axis is contiguous) and either 16-bit type.
+ *
+ * exattn_dtype -- element type of every Q, K, V, O, dO, dQ, dK, dV of one
+ *   call: EXATTN_DTYPE_BF16 (__nv_bfloat16) or EXATTN_DTYPE_F16 (__half).
+ *   The tensor cores multiply that type and accumulate in fp32; P (and dS in
+ *   the backward) are rounded to the same type; outputs are rounded to it.
+ * exattn_strides -- element strides (not bytes) of a tensor seen as
+ *   [B, H, N, d] with d contiguous: element (b, h, n, c) is at
+ *   base[b*b_stride + h*h_stride + n*n_stride + c].  Every stride must be a
+ *   multiple of 8 elements (16 bytes, the tensor-memory-accelerator rule),
+ *   at least 0 and below 2^36, and nonzero along an axis of extent > 1
+ *   (else EXATTN_ERR_ALIGN / EXATTN_ERR_SHAPE).  Contiguous [B, H, N, d] is
+ *   {H*N*d, N*d, d}; contiguous [B, N, H, d] is {N*H*d, d, H*d}.  Rows of an
+ *   output that overlap give undefined results.
+ */
+typedef enum { EXATTN_DTYPE_BF16 = 0, EXATTN_DTYPE_F16 = 1 } exattn_dtype;
+
+typedef struct {
+  long long b_stride;
+  long long h_stride;
+  long long n_stride;
+} exattn_strides;
+
+/*
+ * attn_fwd_ex -- attn_fwd for any exattn_dtype and strided Q, K, V, O
+ *   (lse stays fp32 contiguous [B, H, N]).  Results and errors as attn_fwd;
+ *   an unknown dtype returns EXATTN_ERR_UNSUPPORTED.
+ */
+int attn_fwd_ex(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                const void* v, exattn_strides v_strides, void* o, exattn_strides o_strides, float* lse, int B,
+                int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * attn_bwd_ex -- attn_bwd for any exattn_dtype and strided Q, K, V, O, dO,
+ *   dQ, dK, dV (lse and the workspace as for attn_bwd).  Results and errors
+ *   as attn_bwd.
+ */
+int attn_bwd_ex(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                const void* v, exattn_strides v_strides, const void* o, exattn_strides o_strides, const void* dO,
+                exattn_strides do_strides, const float* lse, void* dq, exattn_strides dq_strides, void* dk,
+                exattn_strides dk_strides, void* dv, exattn_strides dv_strides, int B, int H, int N, int d,
+                int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device
  * memory: a plugin given only its input and output buffers by a runtime that
  * owns all device memory, or code on a latency-critical path where an

@@ -37,21 +37,33 @@ def run_gpu(q, k, v, do, causal: bool, scale: float, bwd: bool = True):
     return {n: t.cpu() for n, t in out.items()}
 
 
-def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
-    """Half the spacing of bf16 numbers at |x| (8 significant bits): the error
-    that rounding the exact value to a bf16 output alone can make."""
+def half_ulp(x: np.ndarray, bits: int = 8) -> np.ndarray:
+    """Half the spacing of numbers with `bits` significant bits at |x| (8 for
+    bf16, 11 for f16): the error that rounding the exact value to such an
+    output alone can make."""
     ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
-    return np.exp2(np.floor(np.log2(ax)) - 8.0)
+    return np.exp2(np.floor(np.log2(ax)) - float(bits))
 
 
-def check_fwd(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what=""):
-    """O is bf16, so an exact result rounded to bf16 is already off by up to
-    half a bf16 ulp (0.0156 for |O| in [4, 8)).  The max-abs bound applies to
-    the error beyond that rounding; the raw max-abs error is reported too."""
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    return half_ulp(x, 8)
+
+
+def out_bits(t: torch.Tensor) -> int:
+    """Significant bits of a tensor's 16-bit type."""
+    return 11 if t.dtype == torch.float16 else 8
+
+
+def check_fwd(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what="",
+              bits: int = 8):
+    """O is bf16 (bits = 8) or f16 (bits = 11), so an exact result rounded to
+    it is already off by up to half an ulp (bf16: 0.0156 for |O| in [4, 8)).
+    The max-abs bound applies to the error beyond that rounding; the raw
+    max-abs error is reported too."""
     assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
     assert np.all(np.isfinite(lse_gpu)), f"{what}: non-finite lse"
     err = np.abs(o_gpu - o_ref)
-    beyond = err - bf16_half_ulp(o_ref)
+    beyond = err - half_ulp(o_ref, bits)
     lerr = np.abs(lse_gpu - lse_ref)
     n_raw = int(np.count_nonzero(err > TOL_O_MAX))
     info = (f"{what}: O max {err.max():.3e} (beyond bf16 rounding {beyond.max():.3e}; "
@@ -91,7 +103,7 @@ def full_parity(orc, q, k, v, do, causal: bool, scale: float, bwd: bool = True, 
     res = run_gpu(q, k, v, do, causal, scale, bwd)
     qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
     o_ref, lse_ref = orc.attention_fwd(qf, kf, vf, causal, scale)
-    msg = check_fwd(to_f64(res["o"]), res["lse"].double().numpy(), o_ref, lse_ref, what)
+    msg = check_fwd(to_f64(res["o"]), res["lse"].double().numpy(), o_ref, lse_ref, what, out_bits(res["o"]))
     if bwd:
         dq_ref, dk_ref, dv_ref = orc.attention_bwd(qf, kf, vf, to_f64(do), causal, scale)
         msg += " | " + check_grads([("dQ", to_f64(res["dq"]), dq_ref), ("dK", to_f64(res["dk"]), dk_ref),

@@ -142,3 +142,41 @@ def test_stage_validation(lib):
     assert lib.attn_bwd_dq(*args[:6], None, 1, 1, 8, 64, 0, 0.1, None) == 1
     assert lib.attn_bwd_dq(*args, 1, 1, 8, 128, 1, float("inf"), None) == 9
     assert lib.attn_bwd_dq(*args, -1, 1, 8, 128, 1, 0.1, None) == 2
+
+
+def test_ex_validation(lib):
+    """attn_fwd_ex / attn_bwd_ex reject a bad type code and bad strides before
+    any CUDA call (fake, 16-byte-aligned pointers; nothing is launched)."""
+    from exact_attention_67_gb300._lib import Strides
+    P = [0x10000 * (i + 1) for i in range(10)]
+    B, H, N, d = 1, 2, 8, 64
+    good = Strides(H * N * d, N * d, d)
+    bnhd = Strides(N * H * d, d, H * d)
+
+    def fwd(dt=0, s=(good, good, good, good), d_=d, N_=N):
+        return lib.attn_fwd_ex(dt, P[0], s[0], P[1], s[1], P[2], s[2], P[3], s[3], P[4], B, H, N_, d_, 1, 0.125,
+                               None)
+
+    assert fwd(dt=2) == 4 and fwd(dt=-1) == 4
+    assert fwd(d_=80) == 4
+    assert fwd(s=(good, Strides(H * N * d, N * d, 60), good, good)) == 3   # not a multiple of 8 elements
+    assert fwd(s=(good, good, Strides(-8, N * d, d), good)) == 3          # negative
+    assert fwd(s=(good, good, good, Strides(H * N * d, N * d, 1 << 36))) == 3
+    assert fwd(s=(good, good, good, Strides(H * N * d, N * d, 0))) == 2   # zero along N > 1
+    assert fwd(s=(Strides(0, 0, d), good, good, good), N_=N) == 2         # zero along H = 2
+    assert lib.attn_fwd_ex(0, None, good, P[1], good, P[2], good, P[3], good, P[4], B, H, N, d, 1, 0.125,
+                           None) == 1
+    assert lib.attn_fwd_ex(1, P[0] + 8, bnhd, P[1], good, P[2], good, P[3], good, P[4], B, H, N, d, 1, 0.125,
+                           None) == 3
+
+    def bwd(dt=0, ss=None, ws_bytes=1 << 20, scale=0.125):
+        s = ss or [good] * 8
+        return lib.attn_bwd_ex(dt, P[0], s[0], P[1], s[1], P[2], s[2], P[3], s[3], P[4], s[4], P[5], P[6], s[5],
+                               P[7], s[6], P[8], s[7], B, H, N, d, 0, scale, P[9], ws_bytes, None)
+
+    assert bwd(dt=3) == 4
+    assert bwd(scale=0.0) == 9
+    bad = [good] * 8
+    bad[6] = Strides(H * N * d, N * d + 4, d)
+    assert bwd(ss=bad) == 3
+    assert bwd(ws_bytes=16) == 6
