@@ -71,11 +71,11 @@ class OracleLib:
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         i, d = ctypes.c_int, ctypes.c_double
-        lib.oracle_head_fwd_rows.argtypes = [dp, dp, dp, i, i, i, d, ip, i, dp, dp, i]
+        lib.oracle_head_fwd_rows.argtypes = [dp, dp, dp, i, i, i, i, d, ip, i, dp, dp, i]
         lib.oracle_head_fwd_rows.restype = i
-        lib.oracle_head_fwd_online.argtypes = [dp, dp, dp, i, i, i, d, i, dp, dp]
+        lib.oracle_head_fwd_online.argtypes = [dp, dp, dp, i, i, i, i, d, i, dp, dp]
         lib.oracle_head_fwd_online.restype = i
-        lib.oracle_head_bwd_rows.argtypes = [dp, dp, dp, dp, i, i, i, d, ip, i, ip, i,
+        lib.oracle_head_bwd_rows.argtypes = [dp, dp, dp, dp, i, i, i, i, d, ip, i, ip, i,
                                              dp, dp, dp, dp, dp, i]
         lib.oracle_head_bwd_rows.restype = i
         lib.oracle_default_threads.argtypes = []
@@ -86,8 +86,9 @@ class OracleLib:
     def default_threads(self) -> int:
         return int(self.lib.oracle_default_threads())
 
-    def head_fwd(self, q, k, v, causal: bool, scale: float, rows=None, nthreads=None):
-        """One head: q, k, v are [N, d].  Returns (o[len(rows), d], lse[len(rows)])."""
+    def head_fwd(self, q, k, v, causal: bool, scale: float, rows=None, nthreads=None, window: int = 0):
+        """One head: q, k, v are [N, d].  Returns (o[len(rows), d], lse[len(rows)]).
+        ``window`` W > 0 keeps only keys with i - j < W (and j - i < W when not causal)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         N, dd = q.shape
         assert k.shape == (N, dd) and v.shape == (N, dd)
@@ -96,12 +97,12 @@ class OracleLib:
         lse = np.empty((r.size,), np.float64)
         nt = self.default_threads() if nthreads is None else int(nthreads)
         _check(self.lib.oracle_head_fwd_rows(_dptr(q), _dptr(k), _dptr(v), N, dd,
-                                             int(bool(causal)), float(scale), _iptr(r), r.size,
-                                             _dptr(o), _dptr(lse), nt), "fwd")
+                                             int(bool(causal)), int(window), float(scale), _iptr(r),
+                                             r.size, _dptr(o), _dptr(lse), nt), "fwd")
         return o, lse
 
     def head_bwd(self, q, k, v, dO, causal: bool, scale: float, qrows=None, krows=None,
-                 nthreads=None, want_stats=False):
+                 nthreads=None, want_stats=False, window: int = 0):
         """One head.  Returns (dq[len(qrows), d], dk[len(krows), d], dv[len(krows), d])
         and, if want_stats, also (lse[N], D[N]) (NaN where not computed)."""
         q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
@@ -115,26 +116,26 @@ class OracleLib:
         D = np.empty((N,), np.float64)
         nt = self.default_threads() if nthreads is None else int(nthreads)
         _check(self.lib.oracle_head_bwd_rows(_dptr(q), _dptr(k), _dptr(v), _dptr(dO), N, dd,
-                                             int(bool(causal)), float(scale), _iptr(qr), qr.size,
-                                             _iptr(kr), kr.size, _dptr(dq), _dptr(dk), _dptr(dv),
+                                             int(bool(causal)), int(window), float(scale), _iptr(qr),
+                                             qr.size, _iptr(kr), kr.size, _dptr(dq), _dptr(dk), _dptr(dv),
                                              _dptr(lse), _dptr(D), nt), "bwd")
         if want_stats:
             return dq, dk, dv, lse, D
         return dq, dk, dv
 
-    def head_fwd_online(self, q, k, v, causal: bool, scale: float, tile_cols: int):
+    def head_fwd_online(self, q, k, v, causal: bool, scale: float, tile_cols: int, window: int = 0):
         """One head, one-pass online-softmax forward with key tiles of tile_cols."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         N, dd = q.shape
         o = np.empty((N, dd), np.float64)
         lse = np.empty((N,), np.float64)
         _check(self.lib.oracle_head_fwd_online(_dptr(q), _dptr(k), _dptr(v), N, dd,
-                                               int(bool(causal)), float(scale), int(tile_cols),
-                                               _dptr(o), _dptr(lse)), "fwd_online")
+                                               int(bool(causal)), int(window), float(scale),
+                                               int(tile_cols), _dptr(o), _dptr(lse)), "fwd_online")
         return o, lse
 
     # ---- whole-tensor helpers, [B, H, N, d] ----
-    def attention_fwd(self, q, k, v, causal: bool, scale: float, nthreads=None):
+    def attention_fwd(self, q, k, v, causal: bool, scale: float, nthreads=None, window: int = 0):
         """[B, H, N, d] fp64 -> (O [B, H, N, d], lse [B, H, N]), natural log."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, H, N, dd = q.shape
@@ -143,10 +144,10 @@ class OracleLib:
         for b in range(B):
             for h in range(H):
                 o[b, h], lse[b, h] = self.head_fwd(q[b, h], k[b, h], v[b, h], causal, scale,
-                                                   nthreads=nthreads)
+                                                   nthreads=nthreads, window=window)
         return o, lse
 
-    def attention_bwd(self, q, k, v, dO, causal: bool, scale: float, nthreads=None):
+    def attention_bwd(self, q, k, v, dO, causal: bool, scale: float, nthreads=None, window: int = 0):
         """[B, H, N, d] fp64 -> (dQ, dK, dV), each [B, H, N, d]."""
         q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
         B, H, N, dd = q.shape
@@ -155,10 +156,10 @@ class OracleLib:
             for h in range(H):
                 dq[b, h], dk[b, h], dv[b, h] = self.head_bwd(q[b, h], k[b, h], v[b, h],
                                                              dO[b, h], causal, scale,
-                                                             nthreads=nthreads)
+                                                             nthreads=nthreads, window=window)
         return dq, dk, dv
 
-    def attention_fwd_online(self, q, k, v, causal: bool, scale: float, tile_cols: int):
+    def attention_fwd_online(self, q, k, v, causal: bool, scale: float, tile_cols: int, window: int = 0):
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, H, N, dd = q.shape
         o = np.empty_like(q)
@@ -166,7 +167,7 @@ class OracleLib:
         for b in range(B):
             for h in range(H):
                 o[b, h], lse[b, h] = self.head_fwd_online(q[b, h], k[b, h], v[b, h], causal,
-                                                          scale, tile_cols)
+                                                          scale, tile_cols, window)
         return o, lse
 
 

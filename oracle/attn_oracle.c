@@ -22,6 +22,13 @@
  *               returns lse_i = m_i + ln(l_i): the row max and normaliser that
  *               [G3F] §4 重计算 says are the only statistics kept, folded into
  *               one natural-log number.
+ *               Optional sliding window: [FA3P] §三.1 suggests a hybrid of
+ *               local attention (LocalAttention(window_size=...)) and global
+ *               attention without defining the window.  Reading used here:
+ *               with window W >= 1, key j is visible to query i only if
+ *               i - j < W (W keys ending at the diagonal under the causal
+ *               flag) and, without the causal flag, also j - i < W; W = 0
+ *               means no window.
  *   backward -- the analytic vector-Jacobian product of that forward for a
  *               loss with output gradient dO (textbook softmax VJP; [RED]
  *               §2.2 and §3.2 state parts of it):
@@ -50,7 +57,11 @@
 #include <string.h>
 #include <unistd.h>
 
-static int visible(int causal, int i, int j) { return !causal || j <= i; }
+static int visible(int causal, int window, int i, int j) {
+    if (causal && j > i) return 0;
+    if (window > 0 && (i - j >= window || (!causal && j - i >= window))) return 0;
+    return 1;
+}
 
 static double dot(const double* a, const double* b, int d) {
     double s = 0.0;
@@ -60,11 +71,11 @@ static double dot(const double* a, const double* b, int d) {
 
 /* Scores of row i: s_j = scale * q_i . k_j, -inf where masked.
  * Returns the row max m.  */
-static double row_scores(const double* q, const double* k, int N, int d, int causal,
+static double row_scores(const double* q, const double* k, int N, int d, int causal, int window,
                          double scale, int i, double* s) {
     double m = -INFINITY;
     for (int j = 0; j < N; ++j) {
-        if (visible(causal, i, j)) {
+        if (visible(causal, window, i, j)) {
             s[j] = scale * dot(q + (size_t)i * d, k + (size_t)j * d, d);
             if (s[j] > m) m = s[j];
         } else {
@@ -77,11 +88,11 @@ static double row_scores(const double* q, const double* k, int N, int d, int cau
 /* Three-step forward for one row: probabilities p (length N), output o_i
  * (length d), and lse.  Returns lse. */
 static double row_forward(const double* q, const double* k, const double* v, int N, int d,
-                          int causal, double scale, int i, double* p, double* o_row) {
-    double m = row_scores(q, k, N, d, causal, scale, i, p);
+                          int causal, int window, double scale, int i, double* p, double* o_row) {
+    double m = row_scores(q, k, N, d, causal, window, scale, i, p);
     double l = 0.0;
     for (int j = 0; j < N; ++j) {
-        p[j] = visible(causal, i, j) ? exp(p[j] - m) : 0.0;
+        p[j] = visible(causal, window, i, j) ? exp(p[j] - m) : 0.0;
         l += p[j];
     }
     for (int j = 0; j < N; ++j) p[j] /= l;
@@ -156,7 +167,7 @@ int oracle_default_threads(void) {
 
 typedef struct {
     const double *q, *k, *v;
-    int N, d, causal;
+    int N, d, causal, window;
     double scale;
     const int* rows;
     double *o, *lse;
@@ -165,7 +176,7 @@ typedef struct {
 static int fwd_item(void* c, int item, double* p) {
     fwd_ctx_t* x = (fwd_ctx_t*)c;
     int i = x->rows[item];
-    x->lse[item] = row_forward(x->q, x->k, x->v, x->N, x->d, x->causal, x->scale, i, p,
+    x->lse[item] = row_forward(x->q, x->k, x->v, x->N, x->d, x->causal, x->window, x->scale, i, p,
                                x->o + (size_t)item * x->d);
     return 0;
 }
@@ -173,13 +184,14 @@ static int fwd_item(void* c, int item, double* p) {
 /* Forward rows rows[0..nrows) of one head.  o_rows is nrows x d, lse_rows is
  * nrows; entry r belongs to query rows[r]. */
 int oracle_head_fwd_rows(const double* q, const double* k, const double* v, int N, int d,
-                         int causal, double scale, const int* rows, int nrows,
+                         int causal, int window, double scale, const int* rows, int nrows,
                          double* o_rows, double* lse_rows, int nthreads) {
-    if (!q || !k || !v || N < 1 || d < 1 || nrows < 0 || (nrows && (!rows || !o_rows || !lse_rows)))
+    if (!q || !k || !v || N < 1 || d < 1 || window < 0 || nrows < 0 ||
+        (nrows && (!rows || !o_rows || !lse_rows)))
         return -1;
     for (int r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= N) return -1;
-    fwd_ctx_t x = {q, k, v, N, d, causal, scale, rows, o_rows, lse_rows};
+    fwd_ctx_t x = {q, k, v, N, d, causal, window, scale, rows, o_rows, lse_rows};
     return parallel_for(nrows, nthreads, (size_t)N, fwd_item, &x);
 }
 
@@ -189,8 +201,8 @@ int oracle_head_fwd_rows(const double* q, const double* k, const double* v, int 
  * tile_cols columns.  Single-threaded: it exists to be compared with the
  * three-step form on small inputs. */
 int oracle_head_fwd_online(const double* q, const double* k, const double* v, int N, int d,
-                           int causal, double scale, int tile_cols, double* o, double* lse) {
-    if (!q || !k || !v || !o || !lse || N < 1 || d < 1 || tile_cols < 1) return -1;
+                           int causal, int window, double scale, int tile_cols, double* o, double* lse) {
+    if (!q || !k || !v || !o || !lse || N < 1 || d < 1 || tile_cols < 1 || window < 0) return -1;
     double* s = (double*)malloc(sizeof(double) * (size_t)tile_cols);
     double* acc = (double*)malloc(sizeof(double) * (size_t)d);
     if (!s || !acc) { free(s); free(acc); return -2; }
@@ -203,7 +215,7 @@ int oracle_head_fwd_online(const double* q, const double* k, const double* v, in
             double m_local = -INFINITY;
             for (int t = 0; t < nt; ++t) {
                 int j = j0 + t;
-                s[t] = visible(causal, i, j)
+                s[t] = visible(causal, window, i, j)
                            ? scale * dot(q + (size_t)i * d, k + (size_t)j * d, d)
                            : -INFINITY;
                 if (s[t] > m_local) m_local = s[t];
@@ -234,7 +246,7 @@ int oracle_head_fwd_online(const double* q, const double* k, const double* v, in
 
 typedef struct {
     const double *q, *k, *v, *dO;
-    int N, d, causal;
+    int N, d, causal, window;
     double scale;
     const int* rows;
     double* lse_all; /* N: lse_i for every row (filled by stats pass) */
@@ -248,14 +260,14 @@ static int stats_item(void* c, int i, double* scratch) {
     bwd_ctx_t* x = (bwd_ctx_t*)c;
     double* p = scratch;
     double* o_row = scratch + x->N;
-    x->lse_all[i] = row_forward(x->q, x->k, x->v, x->N, x->d, x->causal, x->scale, i, p, o_row);
+    x->lse_all[i] = row_forward(x->q, x->k, x->v, x->N, x->d, x->causal, x->window, x->scale, i, p, o_row);
     x->D_all[i] = dot(x->dO + (size_t)i * x->d, o_row, x->d);
     return 0;
 }
 
 /* p_ij from the row statistic: exp(s_ij - lse_i) = exp(s_ij - m_i) / l_i. */
 static double prob(const bwd_ctx_t* x, int i, int j) {
-    if (!visible(x->causal, i, j)) return 0.0;
+    if (!visible(x->causal, x->window, i, j)) return 0.0;
     double s = x->scale * dot(x->q + (size_t)i * x->d, x->k + (size_t)j * x->d, x->d);
     return exp(s - x->lse_all[i]);
 }
@@ -316,11 +328,11 @@ static int stats_list_item(void* c, int item, double* scratch) {
  * non-null, receive those statistics for all N rows (entries not computed
  * are left NaN). */
 int oracle_head_bwd_rows(const double* q, const double* k, const double* v, const double* dO,
-                         int N, int d, int causal, double scale,
+                         int N, int d, int causal, int window, double scale,
                          const int* qrows, int nq, const int* krows, int nk,
                          double* dq_rows, double* dk_rows, double* dv_rows,
                          double* lse_out, double* D_out, int nthreads) {
-    if (!q || !k || !v || !dO || N < 1 || d < 1 || nq < 0 || nk < 0) return -1;
+    if (!q || !k || !v || !dO || N < 1 || d < 1 || window < 0 || nq < 0 || nk < 0) return -1;
     if (nq && (!qrows || !dq_rows)) return -1;
     if (nk && (!krows || !dk_rows || !dv_rows)) return -1;
     for (int r = 0; r < nq; ++r) if (qrows[r] < 0 || qrows[r] >= N) return -1;
@@ -332,7 +344,7 @@ int oracle_head_bwd_rows(const double* q, const double* k, const double* v, cons
     if (!lse_all || !D_all) { free(lse_all); free(D_all); return -2; }
     for (int i = 0; i < N; ++i) { lse_all[i] = NAN; D_all[i] = NAN; }
 
-    bwd_ctx_t x = {q, k, v, dO, N, d, causal, scale, NULL, lse_all, D_all, dq_rows, dk_rows, dv_rows};
+    bwd_ctx_t x = {q, k, v, dO, N, d, causal, window, scale, NULL, lse_all, D_all, dq_rows, dk_rows, dv_rows};
     int rc;
     if (nk > 0) {
         all_rows = (int*)malloc(sizeof(int) * (size_t)N);

@@ -199,5 +199,86 @@ def pin_torch_sdpa(orc, shapes=((1, 2, 256, 64, False), (1, 2, 160, 128, True)))
             assert np.max(np.abs(mine - ref.numpy())) <= 1e-11
 
 
+def _window_counts(N, W, causal):
+    """Visible keys per row under window W (closed form of the reading: i - j < W,
+    and j - i < W when not causal)."""
+    i = np.arange(N)
+    lo = np.maximum(0, i - W + 1)
+    hi = i if causal else np.minimum(N - 1, i + W - 1)
+    return lo, hi, hi - lo + 1
+
+
+def pin_window_identical_keys(orc):
+    """Sliding window, identical keys: every visible score of a row is equal, so
+    o_i is the mean of v over exactly the visible keys and lse_i adds ln(count)."""
+    rng = _rng(21)
+    N, d, scale = 23, 5, 0.7
+    q = rng.standard_normal((N, d))
+    kk = rng.standard_normal(d)
+    k = np.tile(kk, (N, 1))
+    v = rng.standard_normal((N, d))
+    dO = rng.standard_normal((N, d))
+    for causal in (True, False):
+        for W in (1, 2, 5, 22, 23, 40):
+            o, lse = orc.head_fwd(q, k, v, causal, scale, nthreads=3, window=W)
+            lo, hi, cnt = _window_counts(N, W, causal)
+            want_o = np.stack([v[lo[i]:hi[i] + 1].mean(axis=0) for i in range(N)])
+            assert np.max(np.abs(o - want_o)) <= 1e-12, (causal, W)
+            assert np.max(np.abs(lse - (scale * (q @ kk) + np.log(cnt)))) <= 1e-12, (causal, W)
+            dq, dk, dv = orc.head_bwd(q, k, v, dO, causal, scale, nthreads=3, window=W)
+            assert np.max(np.abs(dq)) <= 1e-12
+            # dV_j = sum over the rows that see key j of p_ij dO_i, p_ij = 1/count_i
+            want_dv = np.zeros((N, d))
+            for i in range(N):
+                want_dv[lo[i]:hi[i] + 1] += dO[i] / cnt[i]
+            assert np.max(np.abs(dv - want_dv)) <= 1e-12, (causal, W)
+
+
+def pin_window_one(orc):
+    """Causal window 1: each row sees only its own key, so o_i = v_i exactly and
+    lse_i = s_ii; a window of N or more is no window at all."""
+    rng = _rng(22)
+    N, d, scale = 17, 6, 0.45
+    q, k, v = (2 * rng.standard_normal((N, d)) for _ in range(3))
+    o, lse = orc.head_fwd(q, k, v, True, scale, nthreads=2, window=1)
+    assert np.array_equal(o, v)
+    sii = scale * np.einsum("ij,ij->i", q, k)
+    assert np.max(np.abs(lse - sii)) <= 1e-13 * max(1.0, np.max(np.abs(sii)))
+    for causal in (True, False):
+        o0, l0 = orc.head_fwd(q, k, v, causal, scale, nthreads=2)
+        oN, lN = orc.head_fwd(q, k, v, causal, scale, nthreads=2, window=N)
+        assert np.array_equal(o0, oN) and np.array_equal(l0, lN)
+
+
+def pin_window_online_and_fd(orc):
+    """With a window, the one-pass tiled forward equals the three-step one, and
+    the analytic gradient matches central finite differences."""
+    rng = _rng(23)
+    for N, d, W in ((9, 4, 3), (16, 8, 5)):
+        scale = 1.0 / np.sqrt(d)
+        q, k, v, dO = (rng.standard_normal((N, d)) for _ in range(4))
+        for causal in (True, False):
+            o2, l2 = orc.head_fwd(q, k, v, causal, scale, nthreads=2, window=W)
+            for tile in (1, 3, 16):
+                o1, l1 = orc.head_fwd_online(q, k, v, causal, scale, tile, window=W)
+                assert np.max(np.abs(o1 - o2)) <= 1e-12 and np.max(np.abs(l1 - l2)) <= 1e-12
+            dq, dk, dv = orc.head_bwd(q, k, v, dO, causal, scale, nthreads=2, window=W)
+            h = 1e-6
+            for which, analytic in ((0, dq), (1, dk), (2, dv)):
+                num = np.zeros((N, d))
+                for i in range(N):
+                    for c in range(d):
+                        ap = [q.copy(), k.copy(), v.copy()]
+                        am = [q.copy(), k.copy(), v.copy()]
+                        ap[which][i, c] += h
+                        am[which][i, c] -= h
+                        fp = float(np.sum(dO * orc.head_fwd(*ap, causal, scale, nthreads=1, window=W)[0]))
+                        fm = float(np.sum(dO * orc.head_fwd(*am, causal, scale, nthreads=1, window=W)[0]))
+                        num[i, c] = (fp - fm) / (2 * h)
+                rel = np.linalg.norm(analytic - num) / max(np.linalg.norm(num), 1e-30)
+                assert rel <= 1e-6, (N, d, W, causal, which, rel)
+
+
 ALL_PINS = [pin_normalisation, pin_identical_keys, pin_online, pin_causal_row0, pin_finite_diff,
-            pin_invariants, pin_zero_query, pin_torch_sdpa]
+            pin_invariants, pin_zero_query, pin_torch_sdpa, pin_window_identical_keys, pin_window_one,
+            pin_window_online_and_fd]

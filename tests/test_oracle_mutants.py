@@ -21,11 +21,13 @@ MUTANTS = [
     ("dq_uses_v", "const double* kj = x->k + (size_t)j * d;", "const double* kj = x->v + (size_t)j * d;", 0),
     ("dv_uses_q", "dv[cc] += p * dOi[cc];", "dv[cc] += p * qi[cc];", 0),
     ("D_dropped", "x->D_all[i] = dot(x->dO + (size_t)i * x->d, o_row, x->d);", "x->D_all[i] = 0.0;", 0),
-    ("causal_strict", "return !causal || j <= i;", "return !causal || j < i;", 0),
-    ("causal_plus1", "return !causal || j <= i;", "return !causal || j <= i + 1;", 0),
+    ("causal_strict", "if (causal && j > i) return 0;", "if (causal && j >= i) return 0;", 0),
+    ("causal_plus1", "if (causal && j > i) return 0;", "if (causal && j > i + 1) return 0;", 0),
+    ("window_off_by_one", "(i - j >= window ||", "(i - j > window ||", 0),
+    ("window_one_sided", "(!causal && j - i >= window)", "(0 && j - i >= window)", 0),
     ("lse_log2", "return m + log(l);", "return m + log2(l);", 0),
-    ("no_max_subtract", "p[j] = visible(causal, i, j) ? exp(p[j] - m) : 0.0;",
-     "p[j] = visible(causal, i, j) ? exp(p[j]) : 0.0; m = 0.0;", 0),
+    ("no_max_subtract", "p[j] = visible(causal, window, i, j) ? exp(p[j] - m) : 0.0;",
+     "p[j] = visible(causal, window, i, j) ? exp(p[j]) : 0.0; m = 0.0;", 0),
     ("no_normalise", "for (int j = 0; j < N; ++j) p[j] /= l;", "", 0),
     ("fwd_no_scale", "s[j] = scale * dot(q + (size_t)i * d, k + (size_t)j * d, d);",
      "s[j] = dot(q + (size_t)i * d, k + (size_t)j * d, d);", 0),
