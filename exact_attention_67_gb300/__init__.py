@@ -29,21 +29,25 @@ def _plain(*ts) -> bool:
     return all(t.dtype == torch.bfloat16 and t.is_contiguous() for t in ts)
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None, window: int = 0):
     """Allocate O (same type and memory layout as q) and lse (fp32) with torch
     and run ``attn_fwd`` (contiguous bf16) or ``attn_fwd_ex`` (f16 or strided
-    [B, H, N, d] views, e.g. ``x.transpose(1, 2)`` of a [B, N, H, d] tensor)."""
+    [B, H, N, d] views, e.g. ``x.transpose(1, 2)`` of a [B, N, H, d] tensor, or
+    a sliding ``window`` > 0)."""
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    (attn_fwd if _plain(q, k, v, o) else attn_fwd_ex)(q, k, v, o, lse, causal, s, stream)
+    if window == 0 and _plain(q, k, v, o):
+        attn_fwd(q, k, v, o, lse, causal, s, stream)
+    else:
+        attn_fwd_ex(q, k, v, o, lse, causal, s, stream, window)
     return o, lse
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, stream=None,
-             workspace=None):
+             workspace=None, window: int = 0):
     """Allocate dQ, dK, dV (like q, k, v) and the workspace unless given, and run
     ``attn_bwd`` (contiguous bf16) or ``attn_bwd_ex``."""
     import torch
@@ -53,6 +57,8 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     if workspace is None:
         nbytes = attn_bwd_workspace_size(B, H, N, d, causal)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    fn = attn_bwd if _plain(q, k, v, o, dO, dq, dk, dv) else attn_bwd_ex
-    fn(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
+    if window == 0 and _plain(q, k, v, o, dO, dq, dk, dv):
+        attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
+    else:
+        attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream, window)
     return dq, dk, dv

@@ -72,10 +72,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_dq.restype = i
         S = Strides
-        lib.attn_fwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, i, i, i, i, i, f, vp]
+        lib.attn_fwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, i, i, i, i, i, i, f, vp]
         lib.attn_fwd_ex.restype = i
-        lib.attn_bwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, i, i, i, i, i, f,
-                                    vp, sz, vp]
+        lib.attn_bwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, i, i, i, i, i, i,
+                                    f, vp, sz, vp]
         lib.attn_bwd_ex.restype = i
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_noalloc.restype = i
@@ -147,10 +147,10 @@ def _view4(t: torch.Tensor, name: str):
     return tuple(t.shape), _DTYPES[t.dtype], Strides(t.stride(0), t.stride(1), t.stride(2))
 
 
-def attn_fwd_ex(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+def attn_fwd_ex(q, k, v, o, lse, causal: bool, scale: float, stream=None, window: int = 0) -> None:
     """C ``attn_fwd_ex``: q, k, v, o are [B, H, N, d] views (d contiguous) of one
     type, bf16 or f16 (a [B, N, H, d] tensor passes as ``x.transpose(1, 2)``);
-    lse fp32 contiguous [B, H, N]."""
+    lse fp32 contiguous [B, H, N]; ``window`` > 0 for sliding-window attention."""
     (B, H, N, d), dt, sq = _view4(q, "q")
     views = [_view4(t, n) for n, t in (("k", k), ("v", v), ("o", o))]
     for n, (shape, dtn, _) in zip(("k", "v", "o"), views):
@@ -159,11 +159,14 @@ def attn_fwd_ex(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> Non
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [B, H, N]")
     _check(load().attn_fwd_ex(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o), views[2][2],
-                              _ptr(lse), B, H, N, d, int(bool(causal)), float(scale), _stream(stream)))
+                              _ptr(lse), B, H, N, d, int(bool(causal)), int(window), float(scale),
+                              _stream(stream)))
 
 
-def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
-    """C ``attn_bwd_ex`` on [B, H, N, d] views of one 16-bit type."""
+def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None,
+                window: int = 0) -> None:
+    """C ``attn_bwd_ex`` on [B, H, N, d] views of one 16-bit type (``window`` as
+    in the forward)."""
     (B, H, N, d), dt, sq = _view4(q, "q")
     names = ("k", "v", "o", "dO", "dq", "dk", "dv")
     views = [_view4(t, n) for n, t in zip(names, (k, v, o, dO, dq, dk, dv))]
@@ -176,7 +179,8 @@ def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, wor
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().attn_bwd_ex(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
                               _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], B, H, N, d,
-                              int(bool(causal)), float(scale), _ptr(workspace), ws_bytes, _stream(stream)))
+                              int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
+                              _stream(stream)))
 
 
 def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

@@ -163,7 +163,7 @@ namespace {
 
 int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const Strides& sk, const void* v,
              const Strides& sv, void* o, const Strides& so, float* lse, int B, int H, int N, int d, int causal,
-             float scale, void* stream) {
+             int window, float scale, void* stream) {
   int dev = 0;
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
@@ -185,6 +185,7 @@ int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const S
   a.d = d;
   a.causal = causal ? 1 : 0;
   a.dtype = dtype;
+  a.window = window;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.err = err;
   a.device = dev;
@@ -201,23 +202,24 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return EXATTN_ERR_ALIGN;
   const Strides c = contiguous(H, N, d);
-  return fwd_impl(kBF16, q, c, k, c, v, c, o, c, lse, B, H, N, d, causal, scale, stream);
+  return fwd_impl(kBF16, q, c, k, c, v, c, o, c, lse, B, H, N, d, causal, 0, scale, stream);
 }
 
 extern "C" int attn_fwd_ex(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
                            const void* v, exattn_strides sv, void* o, exattn_strides so, float* lse, int B, int H,
-                           int N, int d, int causal, float scale, void* stream) {
+                           int N, int d, int causal, int window, float scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return EXATTN_ERR_NULL;
   if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
   int rc = check_common(B, H, N, d, scale);
   if (rc != EXATTN_OK) return rc;
+  if (window < 0) return EXATTN_ERR_VALUE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return EXATTN_ERR_ALIGN;
   const exattn_strides* all[4] = {&sq, &sk, &sv, &so};
   for (const exattn_strides* s : all)
     if ((rc = check_strides(*s, B, H, N)) != EXATTN_OK) return rc;
   return fwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, q, to_strides(sq), k, to_strides(sk), v, to_strides(sv),
-                  o, to_strides(so), lse, B, H, N, d, causal, scale, stream);
+                  o, to_strides(so), lse, B, H, N, d, causal, window, scale, stream);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d, int causal) {
@@ -242,7 +244,7 @@ struct BwdInputs {
 };
 
 int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, int H, int N, int d, int causal,
-              float scale) {
+              float scale, int window = 0) {
   int dev = 0;
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
@@ -267,6 +269,7 @@ int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, 
   a.d = d;
   a.causal = causal ? 1 : 0;
   a.dtype = dtype;
+  a.window = window;
   a.scale = scale;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.err = err;
@@ -282,10 +285,10 @@ BwdInputs contiguous_inputs(const void* q, const void* k, const void* v, const v
 // The whole backward: D_i, then dK/dV, then dQ, on one stream.
 int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, const Strides& sdo, const float* lse,
              void* dq, const Strides& sdq, void* dk, const Strides& sdk, void* dv, const Strides& sdv, int B, int H,
-             int N, int d, int causal, float scale, void* workspace, void* stream) {
+             int N, int d, int causal, int window, float scale, void* workspace, void* stream) {
   BwdArgs a{};
   BwdMaps maps;
-  int rc = bwd_setup(a, maps, dtype, in, B, H, N, d, causal, scale);
+  int rc = bwd_setup(a, maps, dtype, in, B, H, N, d, causal, scale, window);
   if (rc != EXATTN_OK) return rc;
   a.o = o;
   a.so = so;
@@ -383,18 +386,19 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
   const Strides c = contiguous(H, N, d);
   return bwd_impl(kBF16, contiguous_inputs(q, k, v, dO, H, N, d), o, c, c, lse, dq, c, dk, c, dv, c, B, H, N, d,
-                  causal, scale, workspace, stream);
+                  causal, 0, scale, workspace, stream);
 }
 
 extern "C" int attn_bwd_ex(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
                            const void* v, exattn_strides sv, const void* o, exattn_strides so, const void* dO,
                            exattn_strides sdo, const float* lse, void* dq, exattn_strides sdq, void* dk,
                            exattn_strides sdk, void* dv, exattn_strides sdv, int B, int H, int N, int d, int causal,
-                           float scale, void* workspace, size_t workspace_bytes, void* stream) {
+                           int window, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return EXATTN_ERR_NULL;
   if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
   int rc = check_common(B, H, N, d, scale);
   if (rc != EXATTN_OK) return rc;
+  if (window < 0) return EXATTN_ERR_VALUE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return EXATTN_ERR_ALIGN;
@@ -405,8 +409,8 @@ extern "C" int attn_bwd_ex(int dtype, const void* q, exattn_strides sq, const vo
   if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
   const BwdInputs in{{q, k, v, dO}, {to_strides(sq), to_strides(sk), to_strides(sv), to_strides(sdo)}};
   return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, o, to_strides(so), to_strides(sdo), lse, dq,
-                  to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, N, d, causal, scale, workspace,
-                  stream);
+                  to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, N, d, causal, window, scale,
+                  workspace, stream);
 }
 
 extern "C" const char* exattn_status_string(int status) {

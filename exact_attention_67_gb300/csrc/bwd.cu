@@ -32,7 +32,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o, Strides so,
                                                          const T* __restrict__ dO, Strides sdo,
-                                                         float* __restrict__ Dout, long long rows, int N, int H) {
+                                                         float* __restrict__ Dout, long long rows, int N, int H,
+                                                         bool contiguous) {
   constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
   constexpr int RPW = 32 / TPR;
   const int lane = threadIdx.x & 31;
@@ -43,10 +44,16 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o
     const long long r = r0 + sub;  // row of [B*H, N]
     float acc = 0.f;
     if (r < rows) {
-      // B*H*N < 2^31 (checked at the C ABI): 32-bit index arithmetic.
-      const int ri = static_cast<int>(r), bh = ri / N, n = ri - bh * N, b = bh / H, h = bh - b * H;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + b * so.b + h * so.h + n * so.n) + part);
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(dO + b * sdo.b + h * sdo.h + n * sdo.n) + part);
+      const T* orow = o + r * D;
+      const T* drow = dO + r * D;
+      if (!contiguous) {
+        // B*H*N < 2^31 (checked at the C ABI): 32-bit index arithmetic.
+        const int ri = static_cast<int>(r), bh = ri / N, n = ri - bh * N, b = bh / H, h = bh - b * H;
+        orow = o + b * so.b + h * so.h + n * so.n;
+        drow = dO + b * sdo.b + h * sdo.h + n * sdo.n;
+      }
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(orow) + part);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(drow) + part);
       const uint32_t* a2 = reinterpret_cast<const uint32_t*>(&a);
       const uint32_t* c2 = reinterpret_cast<const uint32_t*>(&c);
 #pragma unroll
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dk, Strides sdk,
-                    T* __restrict__ dv, Strides sdv, int N, int H, int BH, int n_ktiles, float scale,
+                    T* __restrict__ dv, Strides sdv, int N, int H, int BH, int n_ktiles, int window, float scale,
                     float scale_log2, unsigned* err) {
   using C = DkdvCfg<D>;
   using E = Elem<T>;
@@ -121,9 +128,14 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
   const int k0 = kt * C::BM;
-  const int nq_total = (N + C::BR - 1) / C::BR;
-  const int i_begin = CAUSAL ? (k0 / C::BR) : 0;
-  const int nq = nq_total - i_begin;  // >= 1 since k0 < N
+  // Queries that see some key of [k0, k0 + BM): from the diagonal (causal) or
+  // the window, up to window - 1 past the tile's last key (window W > 0: key j
+  // visible to query i iff i - j < W, and also j - i < W without the causal
+  // mask).
+  const int q_begin = CAUSAL ? k0 : (window > 0 ? max(0, k0 - window + 1) : 0);
+  const int q_end = window > 0 ? min(N, min(N, k0 + C::BM) - 1 + window) : N;  // exclusive
+  const int i_begin = q_begin / C::BR;
+  const int nq = (q_end + C::BR - 1) / C::BR - i_begin;  // >= 1 since k0 < N
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -319,7 +331,22 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       const float* st_lse2 = stat + s * 2 * C::BR;
       const float* st_D = st_lse2 + C::BR;
       const int qi0 = (i_begin + it) * C::BR;
-      const bool need_mask = CAUSAL && (qi0 < k0 + C::BM);
+      // Some query of this step cannot see some key of the tile: before the
+      // diagonal, or outside the window.
+      const bool need_mask = (CAUSAL && qi0 < k0 + C::BM) ||
+                             (window > 0 && (qi0 + C::BR - 1 - k0 >= window ||
+                                             (!CAUSAL && k0 + C::BM - 1 - qi0 >= window)));
+      if (need_mask) {
+        // Hidden scores become -inf, so P = 0 and dS = 0 there.  Query
+        // qi0 + c sees this thread's key iff c lies in [c_lo, c_hi].
+        const int c_lo = (CAUSAL ? key : (window > 0 ? key - window + 1 : -C::BR)) - qi0;
+        const int c_hi = (window > 0 ? key + window - 1 : qi0 + C::BR) - qi0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (h * 32 + e < c_lo || h * 32 + e > c_hi) sr[h][e] = __float_as_uint(-INFINITY);
+      }
       // Column statistics come from shared memory as float4 broadcasts: four
       // columns per load keeps the shared-memory pipe free for the TMA and
       // TMEM traffic of the other roles.
@@ -336,9 +363,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const int cl = 4 * q4 + w;  // column within this half
-            const int c = h * 32 + cl;
-            float p = ex2(fmaf(__uint_as_float(sr[h][cl]), scale_log2, -Lv[w]));
-            if (need_mask && qi0 + c < key) p = 0.f;
+            const float p = ex2(fmaf(__uint_as_float(sr[h][cl]), scale_log2, -Lv[w]));
             pv[w] = p;
             dsv[w] = p * (__uint_as_float(dr[h][cl]) - Dv[w]);
           }
@@ -399,7 +424,9 @@ static cudaError_t launch_prep_t(const BwdArgs& a, cudaStream_t stream) {
   long long blocks = (rows + rpb - 1) / rpb;
   if (blocks > 152 * 16) blocks = 152 * 16;
   bwd_rowdot_kernel<T, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.D, rows, a.N, a.H);
+      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.D, rows, a.N, a.H,
+      a.so.n == D && a.so.h == static_cast<long long>(a.N) * D && a.so.b == static_cast<long long>(a.H) * a.N * D &&
+          a.sdo.n == a.so.n && a.sdo.h == a.so.h && a.sdo.b == a.so.b);
   return cudaGetLastError();
 }
 
@@ -412,7 +439,7 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   const int n_kt = (a.N + C::BM - 1) / C::BM;
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
-      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, a.scale, a.scale_log2, a.err);
+      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, a.window, a.scale, a.scale_log2, a.err);
   return cudaGetLastError();
 }
 

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dq, Strides sdq,
-                  int N, int H, int BH, int n_pairs, float scale, float scale_log2, unsigned* err) {
+                  int N, int H, int BH, int n_pairs, int window, float scale, float scale_log2, unsigned* err) {
   using C = DqCfg<D>;
   using E = Elem<T>;
   using Bars = DqBars<C::STAGES>;
@@ -90,11 +90,20 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
   const int q0 = pair * 2 * C::BM;
-  const int nk_total = (N + C::BN - 1) / C::BN;
-  // Key steps of query tile t (0 if the tile lies wholly past N).
+  // Keys any row of query tile t can see (as in the forward): up to the
+  // diagonal or window - 1 past its last row, from the window start of the
+  // pair's first row; both tiles stream key steps from kv_lo.
+  auto key_end = [&](int t) {  // exclusive
+    const int r0 = q0 + t * C::BM, r1 = min(N, r0 + C::BM);
+    if (r0 >= N) return 0;
+    if (CAUSAL) return r1;
+    return window > 0 ? min(N, r1 - 1 + window) : N;
+  };
+  const int kv_lo = window > 0 ? max(0, q0 - window + 1) / C::BN : 0;
+  // Key steps of query tile t, counted from kv_lo (0 if the tile lies wholly past N).
   auto steps_for = [&](int t) {
-    const int r0 = q0 + t * C::BM;
-    return (r0 >= N) ? 0 : (CAUSAL ? min(nk_total, (r0 + C::BM - 1) / C::BN + 1) : nk_total);
+    const int e = key_end(t);
+    return e == 0 ? 0 : (e + C::BN - 1) / C::BN - kv_lo;
   };
   const int nk0 = steps_for(0), nk1 = steps_for(1);
   const int n_iter = max(nk0, nk1);
@@ -152,9 +161,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_4d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      it * C::BN, hh, bb, pol_keep);
+                      (kv_lo + it) * C::BN, hh, bb, pol_keep);
           tma_load_4d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      it * C::BN, hh, bb, pol_keep);
+                      (kv_lo + it) * C::BN, hh, bb, pol_keep);
         }
         issued = it + 1;
       }
@@ -290,10 +299,23 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tmem_ld32(tbase + C::TM_DP, dr[0]);
       tmem_ld32(tbase + C::TM_DP + 32, dr[1]);
       tmem_wait_ld();
-      const int kj0 = it * C::BN;
-      const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > tile_r0) || (kj0 + C::BN > N);
-      int lim = N - kj0;
-      if (CAUSAL) lim = min(lim, qrow - kj0 + 1);
+      const int kj0 = (kv_lo + it) * C::BN;
+      const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > tile_r0) || (kj0 + C::BN > N) ||
+                             (window > 0 && (kj0 < tile_r0 + C::BM - window ||
+                                             (!CAUSAL && kj0 + C::BN - 1 > tile_r0 + window - 1)));
+      if (need_mask) {
+        // Hidden scores become -inf, so P = 0 and dS = 0 there: key column c
+        // is visible to this row iff lo <= c < lim.
+        int lim = N - kj0;
+        if (CAUSAL) lim = min(lim, qrow - kj0 + 1);
+        else if (window > 0) lim = min(lim, qrow + window - kj0);
+        const int lo = window > 0 ? qrow - window + 1 - kj0 : 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (h * 32 + e >= lim || h * 32 + e < lo) sr[h][e] = __float_as_uint(-INFINITY);
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[16];
@@ -302,9 +324,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           float dsv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int c = h * 32 + 2 * e + u;
-            float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, neg_lse2));
-            if (need_mask && c >= lim) p = 0.f;
+            const float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, neg_lse2));
             dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - Drow);
           }
           pk[e] = E::pack(dsv[0], dsv[1]);
@@ -354,7 +374,7 @@ static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<T*>(a.dq), a.sdq, a.N, a.H,
-      a.BH, n_pairs, a.scale, a.scale_log2, a.err);
+      a.BH, n_pairs, a.window, a.scale, a.scale_log2, a.err);
   return cudaGetLastError();
 }
 

@@ -71,7 +71,7 @@ template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
-                    float* __restrict__ lse_out, int N, int H, int BH, int n_pairs, float scale_log2,
+                    float* __restrict__ lse_out, int N, int H, int BH, int n_pairs, int window, float scale_log2,
                     unsigned* err) {
   using C = FwdCfg<D>;
   using E = Elem<T>;
@@ -88,11 +88,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
   const int q0 = pair * 2 * C::BM;
-  const int nkv_total = (N + C::BN - 1) / C::BN;
-  // Key tiles visited by query tile t (0 if the tile lies wholly past N).
+  // Keys any row of a query tile can see: up to the diagonal (causal) or
+  // window - 1 past its last row (window W > 0: key j visible to query i iff
+  // i - j < W, and also j - i < W without the causal mask), and from the
+  // first row's window start.  Both tiles of the CTA stream key tiles from
+  // the first tile of query tile 0 (kv_lo), tile 1 at most one tile early.
+  auto key_end = [&](int t) {  // exclusive
+    const int r0 = q0 + t * C::BM, r1 = min(N, r0 + C::BM);
+    if (r0 >= N) return 0;
+    if (CAUSAL) return r1;
+    return window > 0 ? min(N, r1 - 1 + window) : N;
+  };
+  const int kv_lo = window > 0 ? max(0, q0 - window + 1) / C::BN : 0;
+  // Key tiles visited by query tile t, counted from kv_lo (0 if the tile lies wholly past N).
   auto tiles_for = [&](int t) {
-    const int r0 = q0 + t * C::BM;
-    return (r0 >= N) ? 0 : (CAUSAL ? min(nkv_total, r0 / C::BN + 1) : nkv_total);
+    const int e = key_end(t);
+    return e == 0 ? 0 : (e + C::BN - 1) / C::BN - kv_lo;
   };
   const int nkv0 = tiles_for(0), nkv1 = tiles_for(1);
   const int n_iter = max(nkv0, nkv1);
@@ -149,14 +160,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(&tm_k, &bars->k_full[s], smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      j * C::BN, hh, bb, pol_kv);
+                      (kv_lo + j) * C::BN, hh, bb, pol_kv);
         issued_k = j + 1;
         if (!mbar_wait(&bars->v_empty[s], ph ^ 1, wc)) break;
         EXATTN_TRACE_POINT(0, j, 1);
         mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(&tm_v, &bars->v_full[s], smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      j * C::BN, hh, bb, pol_kv);
+                      (kv_lo + j) * C::BN, hh, bb, pol_kv);
         issued_v = j + 1;
       }
       if (*reinterpret_cast<volatile int*>(&bars->abort)) {
@@ -294,16 +305,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
       tmem_wait_ld();
 
-      const int kv0 = j * C::BN;
-      const bool need_mask = (CAUSAL && j == (t == 0 ? nkv0 : nkv1) - 1) || (kv0 + C::BN > N);
+      const int kv0 = (kv_lo + j) * C::BN;
+      const int tr0 = q0 + t * C::BM;  // first row of this query tile
+      // Some key of this tile is hidden from some row of the query tile: past
+      // the diagonal, past N, or outside a row's window.
+      const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > tr0) || (kv0 + C::BN > N) ||
+                             (window > 0 && (kv0 < tr0 + C::BM - window ||
+                                             (!CAUSAL && kv0 + C::BN - 1 > tr0 + window - 1)));
       if (need_mask) {
-        int lim = N - kv0;
+        int lim = N - kv0;  // visible columns c: lo <= c < lim
         if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
+        else if (window > 0) lim = min(lim, row_g + window - kv0);
+        const int lo = window > 0 ? row_g - window + 1 - kv0 : 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+            if (c * 32 + e >= lim || c * 32 + e < lo) sr[c][e] = __float_as_uint(-INFINITY);
       }
       // Row max as eight independent chains of three-input maxima: the
       // reduction is exact in any order, and a short chain keeps the
@@ -334,7 +352,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           m_ref = m_new;
         }
       }
-      const float neg_m = -m_ref;
+      // A row that has seen only masked keys so far (a window start inside a
+      // later tile) keeps m_ref = -inf: its P is 0, never NaN.
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
       // Packed partial sums: short FADD chains, half the instructions.
       float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
@@ -421,8 +441,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long grid = static_cast<long long>(n_pairs) * a.BH;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, a.scale_log2,
-      a.err);
+      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, a.window,
+      a.scale_log2, a.err);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ struct FwdArgs {
   Strides so;
   float* lse;               // fp32 [B*H, N]
   int N, H, BH, d, causal, dtype;
+  int window;               // 0, or W >= 1: key j visible to query i iff i - j < W (and j - i < W if not causal)
   float scale_log2;         // scale * log2(e)
   unsigned* err;            // device watchdog word
   int device;
@@ -51,6 +52,7 @@ struct BwdArgs {
   const float* lse;         // fp32 [B*H, N], natural log
   float* D;                 // workspace: fp32 [B*H, N]
   int N, H, BH, d, causal, dtype;
+  int window;               // as FwdArgs::window
   float scale, scale_log2;
   unsigned* err;
   int device;

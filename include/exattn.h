@@ -153,24 +153,33 @@ typedef struct {
 } exattn_strides;
 
 /*
- * attn_fwd_ex -- attn_fwd for any exattn_dtype and strided Q, K, V, O
- *   (lse stays fp32 contiguous [B, H, N]).  Results and errors as attn_fwd;
- *   an unknown dtype returns EXATTN_ERR_UNSUPPORTED.
+ * window -- sliding-window (local) attention for the _ex calls.  The
+ *   "Flash Attention V3：大模型加速的核心网络算子优化实践" page, §三.1, pairs
+ *   local attention (LocalAttention(window_size=...)) with global attention
+ *   without defining the window; here window = W >= 1 lets query i see key j
+ *   only if i - j < W (the W keys ending at the diagonal under the causal
+ *   mask) and, without the causal mask, also j - i < W.  window = 0 is no
+ *   window; a negative window returns EXATTN_ERR_VALUE.  Key tiles wholly
+ *   outside every row's window are skipped.
+ *
+ * attn_fwd_ex -- attn_fwd for any exattn_dtype, strided Q, K, V, O and an
+ *   optional window (lse stays fp32 contiguous [B, H, N]).  Results and
+ *   errors as attn_fwd; an unknown dtype returns EXATTN_ERR_UNSUPPORTED.
  */
 int attn_fwd_ex(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
                 const void* v, exattn_strides v_strides, void* o, exattn_strides o_strides, float* lse, int B,
-                int H, int N, int d, int causal, float scale, void* stream);
+                int H, int N, int d, int causal, int window, float scale, void* stream);
 
 /*
- * attn_bwd_ex -- attn_bwd for any exattn_dtype and strided Q, K, V, O, dO,
- *   dQ, dK, dV (lse and the workspace as for attn_bwd).  Results and errors
- *   as attn_bwd.
+ * attn_bwd_ex -- attn_bwd for any exattn_dtype, strided Q, K, V, O, dO, dQ,
+ *   dK, dV and the window the forward used (lse and the workspace as for
+ *   attn_bwd).  Results and errors as attn_bwd.
  */
 int attn_bwd_ex(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
                 const void* v, exattn_strides v_strides, const void* o, exattn_strides o_strides, const void* dO,
                 exattn_strides do_strides, const float* lse, void* dq, exattn_strides dq_strides, void* dk,
                 exattn_strides dk_strides, void* dv, exattn_strides dv_strides, int B, int H, int N, int d,
-                int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+                int causal, int window, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device

@@ -153,28 +153,30 @@ def test_ex_validation(lib):
     good = Strides(H * N * d, N * d, d)
     bnhd = Strides(N * H * d, d, H * d)
 
-    def fwd(dt=0, s=(good, good, good, good), d_=d, N_=N):
-        return lib.attn_fwd_ex(dt, P[0], s[0], P[1], s[1], P[2], s[2], P[3], s[3], P[4], B, H, N_, d_, 1, 0.125,
-                               None)
+    def fwd(dt=0, s=(good, good, good, good), d_=d, N_=N, window=0):
+        return lib.attn_fwd_ex(dt, P[0], s[0], P[1], s[1], P[2], s[2], P[3], s[3], P[4], B, H, N_, d_, 1, window,
+                               0.125, None)
 
     assert fwd(dt=2) == 4 and fwd(dt=-1) == 4
+    assert fwd(window=-1) == 9
     assert fwd(d_=80) == 4
     assert fwd(s=(good, Strides(H * N * d, N * d, 60), good, good)) == 3   # not a multiple of 8 elements
     assert fwd(s=(good, good, Strides(-8, N * d, d), good)) == 3          # negative
     assert fwd(s=(good, good, good, Strides(H * N * d, N * d, 1 << 36))) == 3
     assert fwd(s=(good, good, good, Strides(H * N * d, N * d, 0))) == 2   # zero along N > 1
     assert fwd(s=(Strides(0, 0, d), good, good, good), N_=N) == 2         # zero along H = 2
-    assert lib.attn_fwd_ex(0, None, good, P[1], good, P[2], good, P[3], good, P[4], B, H, N, d, 1, 0.125,
+    assert lib.attn_fwd_ex(0, None, good, P[1], good, P[2], good, P[3], good, P[4], B, H, N, d, 1, 0, 0.125,
                            None) == 1
-    assert lib.attn_fwd_ex(1, P[0] + 8, bnhd, P[1], good, P[2], good, P[3], good, P[4], B, H, N, d, 1, 0.125,
+    assert lib.attn_fwd_ex(1, P[0] + 8, bnhd, P[1], good, P[2], good, P[3], good, P[4], B, H, N, d, 1, 0, 0.125,
                            None) == 3
 
-    def bwd(dt=0, ss=None, ws_bytes=1 << 20, scale=0.125):
+    def bwd(dt=0, ss=None, ws_bytes=1 << 20, scale=0.125, window=0):
         s = ss or [good] * 8
         return lib.attn_bwd_ex(dt, P[0], s[0], P[1], s[1], P[2], s[2], P[3], s[3], P[4], s[4], P[5], P[6], s[5],
-                               P[7], s[6], P[8], s[7], B, H, N, d, 0, scale, P[9], ws_bytes, None)
+                               P[7], s[6], P[8], s[7], B, H, N, d, 0, window, scale, P[9], ws_bytes, None)
 
     assert bwd(dt=3) == 4
+    assert bwd(window=-5) == 9
     assert bwd(scale=0.0) == 9
     bad = [good] * 8
     bad[6] = Strides(H * N * d, N * d + 4, d)

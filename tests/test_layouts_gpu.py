@@ -41,27 +41,27 @@ def empty_like_layout(x: torch.Tensor, layout: str) -> torch.Tensor:
     return place(torch.empty(x.shape, dtype=x.dtype), layout).fill_(float("nan"))
 
 
-def run_ex(ins, causal, scale, layouts):
+def run_ex(ins, causal, scale, layouts, window=0):
     """attn_fwd_ex + attn_bwd_ex with q, k, v, dO and every output in the given layouts."""
     import exact_attention_67_gb300 as ex
     q, k, v, do = (place(t, lay) for t, lay in zip(ins, layouts[:4]))
     B, H, N, d = q.shape
     o = empty_like_layout(ins[0], layouts[4])
     lse = torch.empty(B, H, N, dtype=torch.float32, device=DEV)
-    ex.attn_fwd_ex(q, k, v, o, lse, causal, scale)
+    ex.attn_fwd_ex(q, k, v, o, lse, causal, scale, window=window)
     dq, dk, dv = (empty_like_layout(ins[0], lay) for lay in layouts[5:8])
     ws = torch.empty(ex.attn_bwd_workspace_size(B, H, N, d, causal), dtype=torch.uint8, device=DEV)
-    ex.attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal, scale, ws)
+    ex.attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal, scale, ws, window=window)
     torch.cuda.synchronize()
     assert ex.device_error() == 0
     return {n: t.cpu() for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
 
 
-def check_against_oracle(orc, ins, res, causal, scale, what):
+def check_against_oracle(orc, ins, res, causal, scale, what, window=0):
     qf, kf, vf, dof = (to_f64(t) for t in ins)
-    o_ref, lse_ref = orc.attention_fwd(qf, kf, vf, causal, scale)
+    o_ref, lse_ref = orc.attention_fwd(qf, kf, vf, causal, scale, window=window)
     msg = check_fwd(to_f64(res["o"]), res["lse"].double().numpy(), o_ref, lse_ref, what, out_bits(res["o"]))
-    dq_ref, dk_ref, dv_ref = orc.attention_bwd(qf, kf, vf, dof, causal, scale)
+    dq_ref, dk_ref, dv_ref = orc.attention_bwd(qf, kf, vf, dof, causal, scale, window=window)
     msg += " | " + check_grads([("dQ", to_f64(res["dq"]), dq_ref), ("dK", to_f64(res["dk"]), dk_ref),
                                 ("dV", to_f64(res["dv"]), dv_ref)], what)
     return msg
