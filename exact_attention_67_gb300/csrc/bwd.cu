@@ -200,10 +200,11 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       const int qi0 = (i_begin + it) * C::BR;
       float* st_lse2 = stat + s * 2 * C::BR;
       float* st_D = st_lse2 + C::BR;
-      st_lse2[lane] = l2a;
-      st_lse2[lane + 32] = l2b;
-      st_D[lane] = dda;
-      st_D[lane + 32] = ddb;
+      // Stored negated, so the elementwise warps add them.
+      st_lse2[lane] = -l2a;
+      st_lse2[lane + 32] = -l2b;
+      st_D[lane] = -dda;
+      st_D[lane + 32] = -ddb;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QTILE);
@@ -358,14 +359,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float4 L4 = st_lse4[h * 8 + q4], D4 = st_D4[h * 8 + q4];
-          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};  // -lse2, -D
           float pv[4], dsv[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const int cl = 4 * q4 + w;  // column within this half
-            const float p = ex2(fmaf(__uint_as_float(sr[h][cl]), scale_log2, -Lv[w]));
-            pv[w] = p;
-            dsv[w] = p * (__uint_as_float(dr[h][cl]) - Dv[w]);
+            pv[w] = ex2(fmaf(__uint_as_float(sr[h][cl]), scale_log2, Lv[w]));
+            dsv[w] = pv[w] * (__uint_as_float(dr[h][cl]) + Dv[w]);
           }
           pk[2 * q4] = E::pack(pv[0], pv[1]);
           pk[2 * q4 + 1] = E::pack(pv[2], pv[3]);

@@ -316,18 +316,20 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           for (int e = 0; e < 32; ++e)
             if (h * 32 + e >= lim || h * 32 + e < lo) sr[h][e] = __float_as_uint(-INFINITY);
       }
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(neg_lse2, neg_lse2);
+      const float2 nD2 = make_float2(-Drow, -Drow);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float p = ex2(fmaf(__uint_as_float(sr[h][2 * e + u]), scale_log2, neg_lse2));
-            dsv[u] = p * (__uint_as_float(dr[h][2 * e + u]) - Drow);
-          }
-          pk[e] = E::pack(dsv[0], dsv[1]);
+          // Packed fp32 pairs: one instruction per two columns.
+          const float2 y = ffma2(make_float2(__uint_as_float(sr[h][2 * e]), __uint_as_float(sr[h][2 * e + 1])),
+                                 sc2, nl2);
+          const float2 p = make_float2(ex2(y.x), ex2(y.y));
+          const float2 dsv = fmul2(p, fadd2(make_float2(__uint_as_float(dr[h][2 * e]),
+                                                        __uint_as_float(dr[h][2 * e + 1])), nD2));
+          pk[e] = E::pack(dsv.x, dsv.y);
         }
         tmem_st16(tbase + C::TM_S + h * 16, pk);  // dS over the first 32 columns of S
       }
