@@ -12,11 +12,12 @@ from __future__ import annotations
 import math
 
 from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
-                   attn_bwd_preprocess, attn_bwd_workspace_size, attn_fwd, attn_fwd_ex, device_error, library_path,
-                   load, status_string, version)
+                   attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_ex,
+                   attn_fwd_varlen, device_error, library_path, load, status_string, version)
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "Strides", "forward", "backward", "device_error",
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward",
+           "backward", "forward_varlen", "backward_varlen", "device_error",
            "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
 
 
@@ -61,4 +62,30 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
         attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
     else:
         attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream, window)
+    return dq, dk, dv
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: float | None = None,
+                   stream=None, window: int = 0):
+    """Packed variable-length forward: q, k, v [total, H, d]; returns O (like q)
+    and lse fp32 [H, total]."""
+    import torch
+    total, H, d = q.shape
+    s = _default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, s, stream, window)
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale: float | None = None, stream=None, window: int = 0, workspace=None):
+    """Packed variable-length backward: returns dQ, dK, dV (like q, k, v)."""
+    import torch
+    total, H, d = q.shape
+    s = _default_scale(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(1, H, total, d, causal), dtype=torch.uint8, device=q.device)
+    attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen, causal, s, workspace, stream, window)
     return dq, dk, dv

@@ -23,7 +23,8 @@ STATUS_NAMES = {
 }
 # Every entry point include/exattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_bwd_noalloc", "exattn_status_string",
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen", "attn_bwd_noalloc",
+           "exattn_status_string",
            "exattn_device_error", "exattn_watchdog_selftest", "exattn_version")
 
 EXATTN_DTYPE_BF16 = 0
@@ -77,6 +78,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, i, i, i, i, i, i,
                                     f, vp, sz, vp]
         lib.attn_bwd_ex.restype = i
+        lib.attn_fwd_varlen.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, vp, i, i, i, i, i, i, i, f, vp]
+        lib.attn_fwd_varlen.restype = i
+        lib.attn_bwd_varlen.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, vp, i, i, i, i,
+                                        i, i, i, f, vp, sz, vp]
+        lib.attn_bwd_varlen.restype = i
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_noalloc.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
@@ -181,6 +187,62 @@ def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, wor
                               _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], B, H, N, d,
                               int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
                               _stream(stream)))
+
+
+def _packed3(t: torch.Tensor, name: str):
+    """Shape, type code and C strides of a packed [total, H, d] tensor (d contiguous)."""
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be a packed [total, H, d] tensor, got {tuple(t.shape)}")
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"{name} must be bfloat16 or float16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.shape[2] > 1 and t.stride(2) != 1:
+        raise ValueError(f"{name}: the d axis must be contiguous")
+    return tuple(t.shape), _DTYPES[t.dtype], Strides(0, t.stride(1), t.stride(0))
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor of B + 1 offsets")
+    return cu_seqlens.numel() - 1
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, scale: float, stream=None,
+                    window: int = 0) -> None:
+    """C ``attn_fwd_varlen``: packed [total, H, d] q, k, v, o of one 16-bit type,
+    lse fp32 [H, total], cu_seqlens int32 [B + 1] on the device."""
+    (total, H, d), dt, sq = _packed3(q, "q")
+    views = [_packed3(t, n) for n, t in (("k", k), ("v", v), ("o", o))]
+    for n, (shape, dtn, _) in zip(("k", "v", "o"), views):
+        if shape != (total, H, d) or dtn != dt:
+            raise ValueError(f"{n} shape/dtype differs from q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [H, total]")
+    B = _cu(cu_seqlens)
+    _check(load().attn_fwd_varlen(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o),
+                                  views[2][2], _ptr(lse), _ptr(cu_seqlens), B, H, int(max_seqlen), total, d,
+                                  int(bool(causal)), int(window), float(scale), _stream(stream)))
+
+
+def attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen: int, causal: bool, scale: float,
+                    workspace, stream=None, window: int = 0) -> None:
+    """C ``attn_bwd_varlen`` on packed [total, H, d] tensors."""
+    (total, H, d), dt, sq = _packed3(q, "q")
+    names = ("k", "v", "o", "dO", "dq", "dk", "dv")
+    views = [_packed3(t, n) for n, t in zip(names, (k, v, o, dO, dq, dk, dv))]
+    for n, (shape, dtn, _) in zip(names, views):
+        if shape != (total, H, d) or dtn != dt:
+            raise ValueError(f"{n} shape/dtype differs from q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [H, total]")
+    B = _cu(cu_seqlens)
+    s = [vw[2] for vw in views]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().attn_bwd_varlen(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
+                                  _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], _ptr(cu_seqlens), B, H,
+                                  int(max_seqlen), total, d, int(bool(causal)), int(window), float(scale),
+                                  _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

@@ -161,18 +161,21 @@ using namespace exattn;
 
 namespace {
 
+// Tensor maps cover [map_b, H, map_n, d]: the batch itself, or (packed
+// variable-length sequences, seq.cu_seqlens set) one batch of seq.total rows.
 int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const Strides& sk, const void* v,
              const Strides& sv, void* o, const Strides& so, float* lse, int B, int H, int N, int d, int causal,
-             int window, float scale, void* stream) {
+             int window, float scale, void* stream, const SeqView& seq = SeqView{nullptr, 0}) {
   int dev = 0;
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
   if (rc != EXATTN_OK) return rc;
+  const int map_b = seq.cu_seqlens ? 1 : B, map_n = seq.cu_seqlens ? seq.total : N;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, dtype, B, H, N, d, sq, 128) || !make_map(&mk, k, dtype, B, H, N, d, sk, 128) ||
-      !make_map(&mv, v, dtype, B, H, N, d, sv, 128))
+  if (!make_map(&mq, q, dtype, map_b, H, map_n, d, sq, 128) || !make_map(&mk, k, dtype, map_b, H, map_n, d, sk, 128) ||
+      !make_map(&mv, v, dtype, map_b, H, map_n, d, sv, 128))
     return EXATTN_ERR_CUDA;
-  FwdArgs a;
+  FwdArgs a{};
   a.tm_q = &mq;
   a.tm_k = &mk;
   a.tm_v = &mv;
@@ -186,6 +189,7 @@ int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const S
   a.causal = causal ? 1 : 0;
   a.dtype = dtype;
   a.window = window;
+  a.seq = seq;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.err = err;
   a.device = dev;
@@ -244,15 +248,16 @@ struct BwdInputs {
 };
 
 int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, int H, int N, int d, int causal,
-              float scale, int window = 0) {
+              float scale, int window = 0, const SeqView& seq = SeqView{nullptr, 0}) {
   int dev = 0;
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
   if (rc != EXATTN_OK) return rc;
+  const int map_b = seq.cu_seqlens ? 1 : B, map_n = seq.cu_seqlens ? seq.total : N;
   for (int i = 0; i < 4; ++i) {
     if (!in.p[i]) continue;
-    if (!make_map(&maps.m[i], in.p[i], dtype, B, H, N, d, in.s[i], 128) ||
-        !make_map(&maps.m[4 + i], in.p[i], dtype, B, H, N, d, in.s[i], 64))
+    if (!make_map(&maps.m[i], in.p[i], dtype, map_b, H, map_n, d, in.s[i], 128) ||
+        !make_map(&maps.m[4 + i], in.p[i], dtype, map_b, H, map_n, d, in.s[i], 64))
       return EXATTN_ERR_CUDA;
   }
   a.tm_q128 = &maps.m[0];
@@ -270,6 +275,7 @@ int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, 
   a.causal = causal ? 1 : 0;
   a.dtype = dtype;
   a.window = window;
+  a.seq = seq;
   a.scale = scale;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.err = err;
@@ -285,10 +291,11 @@ BwdInputs contiguous_inputs(const void* q, const void* k, const void* v, const v
 // The whole backward: D_i, then dK/dV, then dQ, on one stream.
 int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, const Strides& sdo, const float* lse,
              void* dq, const Strides& sdq, void* dk, const Strides& sdk, void* dv, const Strides& sdv, int B, int H,
-             int N, int d, int causal, int window, float scale, void* workspace, void* stream) {
+             int N, int d, int causal, int window, float scale, void* workspace, void* stream,
+             const SeqView& seq = SeqView{nullptr, 0}) {
   BwdArgs a{};
   BwdMaps maps;
-  int rc = bwd_setup(a, maps, dtype, in, B, H, N, d, causal, scale, window);
+  int rc = bwd_setup(a, maps, dtype, in, B, H, N, d, causal, scale, window, seq);
   if (rc != EXATTN_OK) return rc;
   a.o = o;
   a.so = so;
@@ -411,6 +418,61 @@ extern "C" int attn_bwd_ex(int dtype, const void* q, exattn_strides sq, const vo
   return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, o, to_strides(so), to_strides(sdo), lse, dq,
                   to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, N, d, causal, window, scale,
                   workspace, stream);
+}
+
+namespace {
+
+// Shared checks of the packed variable-length calls.
+int check_varlen(const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d, float scale, int window) {
+  if (!cu_seqlens) return EXATTN_ERR_NULL;
+  if (!aligned(cu_seqlens, 4)) return EXATTN_ERR_ALIGN;
+  if (total < 1 || static_cast<long long>(H) * total >= (1ll << 31)) return EXATTN_ERR_SHAPE;
+  if (window < 0) return EXATTN_ERR_VALUE;
+  return check_common(B, H, max_seqlen, d, scale);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_varlen(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                               const void* v, exattn_strides sv, void* o, exattn_strides so, float* lse,
+                               const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d, int causal,
+                               int window, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_varlen(cu_seqlens, B, H, max_seqlen, total, d, scale, window);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  const exattn_strides* all[4] = {&sq, &sk, &sv, &so};
+  for (const exattn_strides* s : all)
+    if ((rc = check_strides(*s, 1, H, total)) != EXATTN_OK) return rc;
+  return fwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, q, to_strides(sq), k, to_strides(sk), v, to_strides(sv),
+                  o, to_strides(so), lse, B, H, max_seqlen, d, causal, window, scale, stream,
+                  SeqView{cu_seqlens, total});
+}
+
+extern "C" int attn_bwd_varlen(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                               const void* v, exattn_strides sv, const void* o, exattn_strides so, const void* dO,
+                               exattn_strides sdo, const float* lse, void* dq, exattn_strides sdq, void* dk,
+                               exattn_strides sdk, void* dv, exattn_strides sdv, const int* cu_seqlens, int B, int H,
+                               int max_seqlen, int total, int d, int causal, int window, float scale,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_varlen(cu_seqlens, B, H, max_seqlen, total, d, scale, window);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  const exattn_strides* all[8] = {&sq, &sk, &sv, &so, &sdo, &sdq, &sdk, &sdv};
+  for (const exattn_strides* s : all)
+    if ((rc = check_strides(*s, 1, H, total)) != EXATTN_OK) return rc;
+  if (!workspace || workspace_bytes < attn_bwd_workspace_size(1, H, total, d, causal)) return EXATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
+  const BwdInputs in{{q, k, v, dO}, {to_strides(sq), to_strides(sk), to_strides(sv), to_strides(sdo)}};
+  return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, o, to_strides(so), to_strides(sdo), lse, dq,
+                  to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, max_seqlen, d, causal, window,
+                  scale, workspace, stream, SeqView{cu_seqlens, total});
 }
 
 extern "C" const char* exattn_status_string(int status) {

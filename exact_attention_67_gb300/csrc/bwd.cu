@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dk, Strides sdk,
-                    T* __restrict__ dv, Strides sdv, int N, int H, int BH, int n_ktiles, int window, float scale,
-                    float scale_log2, unsigned* err) {
+                    T* __restrict__ dv, Strides sdv, int N_max, int H, int BH, int n_ktiles, int window, float scale,
+                    float scale_log2, SeqView seq, unsigned* err) {
   using C = DkdvCfg<D>;
   using E = Elem<T>;
   using Bars = BwdBars<C::STAGES>;
@@ -126,8 +126,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   // Under the causal mask the first key tiles meet the most queries: run them first.
   const int kt = static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
+  const int hh = bh % H, bb = bh / H;  // head and batch index
   const int k0 = kt * C::BM;
+  // This batch's rows (a packed variable-length batch may be shorter than the
+  // grid's longest sequence: such a CTA has nothing to do).
+  const SeqRows sr0 = seq_rows(seq, bb, hh, H, N_max);
+  const int N = sr0.n, row0 = sr0.start, bt = sr0.b_coord;
+  if (k0 >= N) return;
   // Queries that see some key of [k0, k0 + BM): from the diagonal (causal) or
   // the window, up to window - 1 past the tile's last key (window W > 0: key j
   // visible to query i iff i - j < W, and also j - i < W without the causal
@@ -170,8 +175,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KTILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_4d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, k0, hh, bb, pol_keep);
-        tma_load_4d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, k0, hh, bb, pol_keep);
+        tma_load_4d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, row0 + k0, hh, bt, pol_keep);
+        tma_load_4d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, row0 + k0, hh, bt, pol_keep);
       }
     }
     // Row terms of the next step are fetched into registers one step ahead, so
@@ -183,8 +188,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         const int qi = qi0 + lane + 32 * u;
         const bool valid = it < nq && qi < N;
         // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
-        l2[u] = valid ? lse[static_cast<size_t>(bh) * N + qi] * kLog2e : INFINITY;
-        dd[u] = valid ? Dws[static_cast<size_t>(bh) * N + qi] : 0.f;
+        l2[u] = valid ? lse[sr0.stat0 + qi] * kLog2e : INFINITY;
+        dd[u] = valid ? Dws[sr0.stat0 + qi] : 0.f;
       }
     };
     float nl2[2], ndd[2];
@@ -209,9 +214,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_4d(&tm_q, &bars->st_full[s], smem + C::OFF_Q + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, hh, bb,
+          tma_load_4d(&tm_q, &bars->st_full[s], smem + C::OFF_Q + s * C::QTILE + c * C::QCHUNK, c * 64, row0 + qi0, hh, bt,
                       pol_keep);
-          tma_load_4d(&tm_do, &bars->st_full[s], smem + C::OFF_DO + s * C::QTILE + c * C::QCHUNK, c * 64, qi0, hh, bb,
+          tma_load_4d(&tm_do, &bars->st_full[s], smem + C::OFF_DO + s * C::QTILE + c * C::QCHUNK, c * 64, row0 + qi0, hh, bt,
                       pol_keep);
         }
         EXATTN_TRACE_POINT(0, it, 1);
@@ -389,7 +394,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         const uint32_t tacc = tmem + lane_bits + (which == 0 ? C::TM_DK : C::TM_DV);
         const float mul = which == 0 ? scale : 1.f;
         const Strides& so = which == 0 ? sdk : sdv;
-        T* dst_row = (which == 0 ? dk : dv) + bb * so.b + hh * so.h + static_cast<long long>(key) * so.n;
+        T* dst_row = (which == 0 ? dk : dv) + bt * so.b + hh * so.h + static_cast<long long>(row0 + key) * so.n;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -419,14 +424,17 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
 // ---------------------------------------------------------------- launch
 template <typename T, int D>
 static cudaError_t launch_prep_t(const BwdArgs& a, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(a.BH) * a.N;
+  // Packed variable-length sequences are one batch of `total` rows per head.
+  const int n_rows = a.seq.cu_seqlens ? a.seq.total : a.N;
+  const long long rows = static_cast<long long>(a.seq.cu_seqlens ? a.H : a.BH) * n_rows;
   const int rpb = 256 / (D / 8);  // rows per 256-thread block
   long long blocks = (rows + rpb - 1) / rpb;
   if (blocks > 152 * 16) blocks = 152 * 16;
   bwd_rowdot_kernel<T, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.D, rows, a.N, a.H,
-      a.so.n == D && a.so.h == static_cast<long long>(a.N) * D && a.so.b == static_cast<long long>(a.H) * a.N * D &&
-          a.sdo.n == a.so.n && a.sdo.h == a.so.h && a.sdo.b == a.so.b);
+      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.D, rows, n_rows, a.H,
+      a.so.n == D && a.so.h == static_cast<long long>(n_rows) * D &&
+          a.so.b == static_cast<long long>(a.H) * n_rows * D && a.sdo.n == a.so.n && a.sdo.h == a.so.h &&
+          a.sdo.b == a.so.b);
   return cudaGetLastError();
 }
 
@@ -439,7 +447,7 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   const int n_kt = (a.N + C::BM - 1) / C::BM;
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
-      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, a.window, a.scale, a.scale_log2, a.err);
+      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return cudaGetLastError();
 }
 

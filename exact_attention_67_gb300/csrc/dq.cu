@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dq, Strides sdq,
-                  int N, int H, int BH, int n_pairs, int window, float scale, float scale_log2, unsigned* err) {
+                  int N_max, int H, int BH, int n_pairs, int window, float scale, float scale_log2, SeqView seq,
+                  unsigned* err) {
   using C = DqCfg<D>;
   using E = Elem<T>;
   using Bars = DqBars<C::STAGES>;
@@ -88,8 +89,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   // Under the causal mask the last query tiles meet the most keys: run them first.
   const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
+  const int hh = bh % H, bb = bh / H;  // head and batch index
   const int q0 = pair * 2 * C::BM;
+  // This batch's rows (a packed variable-length batch may be shorter than the
+  // grid's longest sequence: such a CTA has nothing to do).
+  const SeqRows sr0 = seq_rows(seq, bb, hh, H, N_max);
+  const int N = sr0.n, row0 = sr0.start, bt = sr0.b_coord;
+  if (q0 >= N) return;
   // Keys any row of query tile t can see (as in the forward): up to the
   // diagonal or window - 1 past its last row, from the window start of the
   // pair's first row; both tiles stream key steps from kv_lo.
@@ -147,9 +153,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->qd_full[t], 2 * C::QTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_4d(&tm_q, &bars->qd_full[t], smem + C::OFF_Q + t * C::QTILE + c * C::QCHUNK, c * 64,
-                      q0 + t * C::BM, hh, bb, pol_once);
+                      row0 + q0 + t * C::BM, hh, bt, pol_once);
           tma_load_4d(&tm_do, &bars->qd_full[t], smem + C::OFF_DO + t * C::QTILE + c * C::QCHUNK, c * 64,
-                      q0 + t * C::BM, hh, bb, pol_once);
+                      row0 + q0 + t * C::BM, hh, bt, pol_once);
         }
       }
       int issued = 0;
@@ -161,9 +167,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::KTILE);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_4d(&tm_k, &bars->st_full[s], smem + C::OFF_K + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      (kv_lo + it) * C::BN, hh, bb, pol_keep);
+                      row0 + (kv_lo + it) * C::BN, hh, bt, pol_keep);
           tma_load_4d(&tm_v, &bars->st_full[s], smem + C::OFF_V + s * C::KTILE + c * C::KCHUNK, c * 64,
-                      (kv_lo + it) * C::BN, hh, bb, pol_keep);
+                      row0 + (kv_lo + it) * C::BN, hh, bt, pol_keep);
         }
         issued = it + 1;
       }
@@ -286,8 +292,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const uint32_t tbase = tmem + lane_bits + t * C::TM_TILE;
     const bool valid = qrow < N;
     // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
-    const float neg_lse2 = valid ? -lse[static_cast<size_t>(bh) * N + qrow] * kLog2eDq : -INFINITY;
-    const float Drow = valid ? Dws[static_cast<size_t>(bh) * N + qrow] : 0.f;
+    const float neg_lse2 = valid ? -lse[sr0.stat0 + qrow] * kLog2eDq : -INFINITY;
+    const float Drow = valid ? Dws[sr0.stat0 + qrow] : 0.f;
     bool ok = nk_t > 0;
     for (int it = 0; ok && it < nk_t; ++it) {
       if (!(ok = mbar_wait(&bars->s_full[t], it & 1, wc))) break;
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     if (ok && nk_t > 0) ok = mbar_wait(&bars->acc_done[t], 0, wc);
     if (ok && nk_t > 0) {
       tc_fence_after();
-      T* dst_row = dq + bb * sdq.b + hh * sdq.h + static_cast<long long>(qrow) * sdq.n;
+      T* dst_row = dq + bt * sdq.b + hh * sdq.h + static_cast<long long>(row0 + qrow) * sdq.n;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -376,7 +382,7 @@ static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<T*>(a.dq), a.sdq, a.N, a.H,
-      a.BH, n_pairs, a.window, a.scale, a.scale_log2, a.err);
+      a.BH, n_pairs, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return cudaGetLastError();
 }
 

@@ -71,8 +71,8 @@ template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
-                    float* __restrict__ lse_out, int N, int H, int BH, int n_pairs, int window, float scale_log2,
-                    unsigned* err) {
+                    float* __restrict__ lse_out, int N_max, int H, int BH, int n_pairs, int window,
+                    float scale_log2, SeqView seq, unsigned* err) {
   using C = FwdCfg<D>;
   using E = Elem<T>;
   using Bars = FwdBars<C::STAGES>;
@@ -86,8 +86,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   // Heaviest work first: under the causal mask the last query pairs see the most keys.
   const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int hh = bh % H, bb = bh / H;  // head and batch index (TMA coordinates)
+  const int hh = bh % H, bb = bh / H;  // head and batch index
   const int q0 = pair * 2 * C::BM;
+  // This batch's rows (a packed variable-length batch may be shorter than the
+  // grid's longest sequence: such a CTA has nothing to do).
+  const SeqRows sr0 = seq_rows(seq, bb, hh, H, N_max);
+  const int N = sr0.n, row0 = sr0.start, bt = sr0.b_coord;
+  if (q0 >= N) return;
   // Keys any row of a query tile can see: up to the diagonal (causal) or
   // window - 1 past its last row (window W > 0: key j visible to query i iff
   // i - j < W, and also j - i < W without the causal mask), and from the
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->q_full[t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(&tm_q, &bars->q_full[t], smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      q0 + t * C::BM, hh, bb, pol_q);
+                      row0 + q0 + t * C::BM, hh, bt, pol_q);
       }
       int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_iter; ++j) {
@@ -160,14 +165,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(&tm_k, &bars->k_full[s], smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      (kv_lo + j) * C::BN, hh, bb, pol_kv);
+                      row0 + (kv_lo + j) * C::BN, hh, bt, pol_kv);
         issued_k = j + 1;
         if (!mbar_wait(&bars->v_empty[s], ph ^ 1, wc)) break;
         EXATTN_TRACE_POINT(0, j, 1);
         mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(&tm_v, &bars->v_full[s], smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, c * 64,
-                      (kv_lo + j) * C::BN, hh, bb, pol_kv);
+                      row0 + (kv_lo + j) * C::BN, hh, bt, pol_kv);
         issued_v = j + 1;
       }
       if (*reinterpret_cast<volatile int*>(&bars->abort)) {
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (ok && (t == 0 ? nkv0 : nkv1) > 0) {
       tc_fence_after();
       const float inv_l = 1.f / lb;
-      T* orow = out + bb * so.b + hh * so.h + static_cast<long long>(row_g) * so.n;
+      T* orow = out + bt * so.b + hh * so.h + static_cast<long long>(row0 + row_g) * so.n;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o_r[32];
@@ -422,7 +427,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (row_g < N) lse_out[static_cast<size_t>(bh) * N + row_g] = (m_ref + log2f(l)) * 0.6931471805599453f;
+      if (row_g < N) lse_out[sr0.stat0 + row_g] = (m_ref + log2f(l)) * 0.6931471805599453f;
     }
   }
 
@@ -442,7 +447,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const long long grid = static_cast<long long>(n_pairs) * a.BH;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, a.window,
-      a.scale_log2, a.err);
+      a.scale_log2, a.seq, a.err);
   return cudaGetLastError();
 }
 

@@ -14,6 +14,42 @@ struct Strides {
 // Element type of Q, K, V, O, dO, dQ, dK, dV (the C ABI's exattn_dtype).
 enum : int { kBF16 = 0, kF16 = 1 };
 
+// Where the rows of batch b live.  Fixed length (cu_seqlens == nullptr):
+// rows [0, N) of batch b, statistics (lse, D) at [b*H + h, N].  Packed
+// variable length: sequence b is rows [cu_seqlens[b], cu_seqlens[b+1]) of
+// one [total, H, d] tensor (batch stride unused), statistics at [h, total].
+struct SeqView {
+  const int* cu_seqlens;  // device, B + 1 non-decreasing offsets, or nullptr
+  int total;              // rows of the packed tensors
+};
+
+// Rows of batch b as seen by one CTA: first row in the tensor, length
+// (clamped to [0, n_max] and to the packed tensor, so a bad offset table can
+// never send an access out of bounds), the batch coordinate of the tensor
+// maps and output strides, and the first statistics index of head h.
+struct SeqRows {
+  int start, n, b_coord;
+  long long stat0;
+};
+
+__device__ __forceinline__ SeqRows seq_rows(const SeqView& sv, int b, int h, int H, int n_max) {
+  SeqRows r;
+  if (!sv.cu_seqlens) {
+    r.start = 0;
+    r.n = n_max;
+    r.b_coord = b;
+    r.stat0 = (static_cast<long long>(b) * H + h) * n_max;
+  } else {
+    const int s0 = min(max(sv.cu_seqlens[b], 0), sv.total);
+    const int s1 = min(max(sv.cu_seqlens[b + 1], s0), sv.total);
+    r.start = s0;
+    r.n = min(s1 - s0, n_max);
+    r.b_coord = 0;
+    r.stat0 = static_cast<long long>(h) * sv.total + s0;
+  }
+  return r;
+}
+
 struct FwdArgs {
   const CUtensorMap* tm_q;  // 4-D maps (d, N, H, B), box 64 x 128 x 1 x 1, 128-byte swizzle
   const CUtensorMap* tm_k;
@@ -23,6 +59,7 @@ struct FwdArgs {
   float* lse;               // fp32 [B*H, N]
   int N, H, BH, d, causal, dtype;
   int window;               // 0, or W >= 1: key j visible to query i iff i - j < W (and j - i < W if not causal)
+  SeqView seq;              // N is the longest sequence when seq.cu_seqlens is set
   float scale_log2;         // scale * log2(e)
   unsigned* err;            // device watchdog word
   int device;
@@ -53,6 +90,7 @@ struct BwdArgs {
   float* D;                 // workspace: fp32 [B*H, N]
   int N, H, BH, d, causal, dtype;
   int window;               // as FwdArgs::window
+  SeqView seq;              // as FwdArgs::seq
   float scale, scale_log2;
   unsigned* err;
   int device;

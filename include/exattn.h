@@ -182,6 +182,41 @@ int attn_bwd_ex(int dtype, const void* q, exattn_strides q_strides, const void* 
                 int causal, int window, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Packed variable-length batches.  The masked_flash_attention sketch of
+ * "Flash Attention V3：大模型加速的核心网络算子优化实践", §三.3, pads
+ * variable-length sequences and masks the padding with a [batch, 1, seq,
+ * seq] tensor; here the sequences are packed instead, so neither the padding
+ * nor an N x N mask exists.
+ *   cu_seqlens : device int32 [B + 1], 4-byte aligned, non-decreasing offsets
+ *                with cu_seqlens[0] = 0 and cu_seqlens[B] = total: sequence b
+ *                is rows [cu_seqlens[b], cu_seqlens[b+1]) of every tensor.
+ *                Offsets are clamped to [0, total] and lengths to max_seqlen
+ *                on the device, so a wrong table gives wrong results but
+ *                never an out-of-bounds access.
+ *   q, k, v, o, dO, dq, dk, dv : [total, H, d] (d contiguous) described by
+ *                exattn_strides with b_stride unused (any multiple of 8),
+ *                h_stride and n_stride (the token stride).
+ *   lse        : fp32 [H, total] (head-major), as is the backward's D.
+ *   max_seqlen : the longest sequence (sizes the grid; 1 <= max_seqlen).
+ *   total      : rows of the packed tensors, H * total < 2^31.
+ * Each sequence is its own attention problem (masks, window and causal
+ * alignment apply within it).  Errors as the _ex calls; a null cu_seqlens
+ * returns EXATTN_ERR_NULL.  attn_bwd_varlen needs a workspace of
+ * attn_bwd_workspace_size(1, H, total, d, causal) bytes.
+ */
+int attn_fwd_varlen(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                    const void* v, exattn_strides v_strides, void* o, exattn_strides o_strides, float* lse,
+                    const int* cu_seqlens, int B, int H, int max_seqlen, int total, int d, int causal, int window,
+                    float scale, void* stream);
+int attn_bwd_varlen(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                    const void* v, exattn_strides v_strides, const void* o, exattn_strides o_strides,
+                    const void* dO, exattn_strides do_strides, const float* lse, void* dq,
+                    exattn_strides dq_strides, void* dk, exattn_strides dk_strides, void* dv,
+                    exattn_strides dv_strides, const int* cu_seqlens, int B, int H, int max_seqlen, int total,
+                    int d, int causal, int window, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
  * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device
  * memory: a plugin given only its input and output buffers by a runtime that
  * owns all device memory, or code on a latency-critical path where an

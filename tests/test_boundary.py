@@ -182,3 +182,30 @@ def test_ex_validation(lib):
     bad[6] = Strides(H * N * d, N * d + 4, d)
     assert bwd(ss=bad) == 3
     assert bwd(ws_bytes=16) == 6
+
+
+def test_varlen_validation(lib):
+    """attn_fwd_varlen / attn_bwd_varlen reject a missing or misaligned offset
+    table and bad sizes before any CUDA call (nothing is launched)."""
+    from exact_attention_67_gb300._lib import Strides
+    P = [0x10000 * (i + 1) for i in range(12)]
+    H, d, total = 2, 64, 40
+    s = Strides(0, d, H * d)
+
+    def fwd(cu=P[5], B=3, maxlen=20, tot=total, window=0, dt=0):
+        return lib.attn_fwd_varlen(dt, P[0], s, P[1], s, P[2], s, P[3], s, P[4], cu, B, H, maxlen, tot, d, 1,
+                                   window, 0.125, None)
+
+    assert fwd(cu=None) == 1
+    assert fwd(cu=P[5] + 2) == 3
+    assert fwd(tot=0) == 2 and fwd(B=0) == 2 and fwd(maxlen=0) == 2
+    assert fwd(window=-1) == 9 and fwd(dt=7) == 4
+    assert lib.attn_fwd_varlen(0, P[0], Strides(0, d, 60), P[1], s, P[2], s, P[3], s, P[4], P[5], 3, H, 20, total,
+                               d, 1, 0, 0.125, None) == 3
+
+    def bwd(cu=P[10], ws=1 << 20):
+        return lib.attn_bwd_varlen(0, P[0], s, P[1], s, P[2], s, P[3], s, P[4], s, P[5], P[6], s, P[7], s, P[8],
+                                   s, cu, 3, H, 20, total, d, 1, 0, 0.125, P[9], ws, None)
+
+    assert bwd(cu=None) == 1
+    assert bwd(ws=8) == 6
