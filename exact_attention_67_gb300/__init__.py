@@ -12,12 +12,14 @@ from __future__ import annotations
 import math
 
 from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
-                   attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_ex,
-                   attn_fwd_varlen, device_error, library_path, load, status_string, version)
+                   attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_decode,
+                   attn_fwd_decode_workspace_size, attn_fwd_ex, attn_fwd_varlen, device_error, library_path, load,
+                   status_string, version)
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward",
-           "backward", "forward_varlen", "backward_varlen", "device_error",
+           "backward", "forward_varlen", "backward_varlen", "attn_fwd_decode", "attn_fwd_decode_workspace_size",
+           "forward_decode", "device_error",
            "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
 
 
@@ -89,3 +91,18 @@ def backward_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen: int, causal: bo
         workspace = torch.empty(attn_bwd_workspace_size(1, H, total, d, causal), dtype=torch.uint8, device=q.device)
     attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen, causal, s, workspace, stream, window)
     return dq, dk, dv
+
+
+def forward_decode(q, k, v, causal: bool = False, scale: float | None = None, stream=None, window: int = 0):
+    """Decode-shaped forward: q [B, H, Nq, d] against k, v [B, H, Nk, d], the
+    queries aligned to the last Nq keys; returns O (like q) and lse [B, H, Nq]."""
+    import torch
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    s = _default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    nbytes = attn_fwd_decode_workspace_size(B, H, Nq, Nk, d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+    attn_fwd_decode(q, k, v, o, lse, causal, s, ws, stream, window)
+    return o, lse

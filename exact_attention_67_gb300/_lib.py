@@ -23,7 +23,8 @@ STATUS_NAMES = {
 }
 # Every entry point include/exattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen", "attn_bwd_noalloc",
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen",
+           "attn_fwd_decode_workspace_size", "attn_fwd_decode", "attn_bwd_noalloc",
            "exattn_status_string",
            "exattn_device_error", "exattn_watchdog_selftest", "exattn_version")
 
@@ -83,6 +84,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_varlen.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, vp, i, i, i, i,
                                         i, i, i, f, vp, sz, vp]
         lib.attn_bwd_varlen.restype = i
+        lib.attn_fwd_decode_workspace_size.argtypes = [i, i, i, i, i]
+        lib.attn_fwd_decode_workspace_size.restype = sz
+        lib.attn_fwd_decode.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.attn_fwd_decode.restype = i
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_noalloc.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
@@ -243,6 +248,31 @@ def attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen: int
                                   _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], _ptr(cu_seqlens), B, H,
                                   int(max_seqlen), total, d, int(bool(causal)), int(window), float(scale),
                                   _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def attn_fwd_decode_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().attn_fwd_decode_workspace_size(B, H, Nq, Nk, d))
+
+
+def attn_fwd_decode(q, k, v, o, lse, causal: bool, scale: float, workspace=None, stream=None,
+                    window: int = 0) -> None:
+    """C ``attn_fwd_decode``: q, o [B, H, Nq, d] and k, v [B, H, Nk, d] views of
+    one 16-bit type (d contiguous), lse fp32 [B, H, Nq]; queries aligned to
+    the last Nq keys."""
+    (B, H, Nq, d), dt, sq = _view4(q, "q")
+    (Bk, Hk, Nk, dk_), dtk, sk = _view4(k, "k")
+    (Bv, Hv, Nv, dv_), dtv, sv = _view4(v, "v")
+    (Bo, Ho, No, do_), dto, so = _view4(o, "o")
+    if (Bk, Hk, dk_) != (B, H, d) or (Bv, Hv, Nv, dv_) != (B, H, Nk, d) or (Bo, Ho, No, do_) != (B, H, Nq, d):
+        raise ValueError("shapes must be q, o [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if len({dt, dtk, dtv, dto}) != 1:
+        raise ValueError("q, k, v, o must share one dtype")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, Nq]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().attn_fwd_decode(dt, _ptr(q), sq, _ptr(k), sk, _ptr(v), sv, _ptr(o), so, _ptr(lse), B, H, Nq, Nk,
+                                  d, int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
+                                  _stream(stream)))
 
 
 def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

@@ -2,6 +2,7 @@
 // argument validation, per-device set-up, TMA tensor-map encoding and kernel
 // launches.  No device memory is allocated here and nothing synchronises
 // except exattn_device_error().
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -473,6 +474,108 @@ extern "C" int attn_bwd_varlen(int dtype, const void* q, exattn_strides sq, cons
   return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, o, to_strides(so), to_strides(sdo), lse, dq,
                   to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, max_seqlen, d, causal, window,
                   scale, workspace, stream, SeqView{cu_seqlens, total});
+}
+
+namespace {
+
+// Key splits of a decode-shaped forward: enough CTAs for about two waves on
+// the 152 SMs, at least two 128-key tiles per split, no empty split.
+struct DecodePlan {
+  int n_splits, tiles_per_split, nq_pad;
+  size_t o_bytes, lse_bytes, total_bytes;
+};
+
+DecodePlan decode_plan(int B, int H, int Nq, int Nk, int d) {
+  const long long nkt = (Nk + 127) / 128;
+  const int n_pairs = (Nq + 255) / 256;
+  const long long base = static_cast<long long>(n_pairs) * B * H;
+  long long splits = std::min(nkt, std::max(1ll, (304 + base - 1) / base));
+  splits = std::min(splits, std::max(1ll, nkt / 2));
+  const long long tps = (nkt + splits - 1) / splits;
+  splits = (nkt + tps - 1) / tps;
+  DecodePlan p{static_cast<int>(splits), static_cast<int>(tps), n_pairs * 256, 0, 0, 0};
+  if (p.n_splits > 1) {
+    const size_t rows = static_cast<size_t>(p.n_splits) * B * H * p.nq_pad;
+    p.o_bytes = (rows * d * sizeof(float) + 255) & ~size_t(255);
+    p.lse_bytes = (rows * sizeof(float) + 255) & ~size_t(255);
+    p.total_bytes = p.o_bytes + 2 * p.lse_bytes;
+  }
+  return p;
+}
+
+int check_decode(int B, int H, int Nq, int Nk, int d, int causal, int window, float scale) {
+  if (Nq < 1 || Nk < 1) return EXATTN_ERR_SHAPE;
+  if ((causal || window > 0) && Nq > Nk) return EXATTN_ERR_SHAPE;  // a query with no key at or before it
+  if (window < 0) return EXATTN_ERR_VALUE;
+  if (static_cast<long long>(B) * H * Nk >= (1ll << 31)) return EXATTN_ERR_SHAPE;
+  return check_common(B, H, Nq, d, scale);
+}
+
+}  // namespace
+
+extern "C" size_t attn_fwd_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode(B, H, Nq, Nk, d, 0, 0, 1.f) != EXATTN_OK) return 0;
+  return decode_plan(B, H, Nq, Nk, d).total_bytes;
+}
+
+extern "C" int attn_fwd_decode(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                               const void* v, exattn_strides sv, void* o, exattn_strides so, float* lse, int B,
+                               int H, int Nq, int Nk, int d, int causal, int window, float scale, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_decode(B, H, Nq, Nk, d, causal, window, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  if ((rc = check_strides(sq, B, H, Nq)) != EXATTN_OK || (rc = check_strides(so, B, H, Nq)) != EXATTN_OK ||
+      (rc = check_strides(sk, B, H, Nk)) != EXATTN_OK || (rc = check_strides(sv, B, H, Nk)) != EXATTN_OK)
+    return rc;
+  const DecodePlan plan = decode_plan(B, H, Nq, Nk, d);
+  if (plan.total_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.total_bytes) return EXATTN_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
+  }
+  int dev = 0;
+  unsigned* err = nullptr;
+  if ((rc = device_setup(&dev, &err)) != EXATTN_OK) return rc;
+  const int dt = dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, dt, B, H, Nq, d, to_strides(sq), 128) || !make_map(&mk, k, dt, B, H, Nk, d, to_strides(sk), 128) ||
+      !make_map(&mv, v, dt, B, H, Nk, d, to_strides(sv), 128))
+    return EXATTN_ERR_CUDA;
+  FwdArgs a{};
+  a.tm_q = &mq;
+  a.tm_k = &mk;
+  a.tm_v = &mv;
+  a.o = o;
+  a.so = to_strides(so);
+  a.lse = lse;
+  a.N = Nq;
+  a.H = H;
+  a.BH = B * H;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.dtype = dt;
+  a.window = window;
+  a.seq = SeqView{nullptr, 0};
+  a.kv.nk = Nk;
+  a.kv.n_splits = plan.n_splits;
+  a.kv.tiles_per_split = plan.tiles_per_split;
+  a.kv.nq_pad = plan.nq_pad;
+  if (plan.n_splits > 1) {
+    char* ws = static_cast<char*>(workspace);
+    a.kv.part_o = reinterpret_cast<float*>(ws);
+    a.kv.part_lse = reinterpret_cast<float*>(ws + plan.o_bytes);
+    a.kv.part_lseb = reinterpret_cast<float*>(ws + plan.o_bytes + plan.lse_bytes);
+  }
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.err = err;
+  a.device = dev;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_fwd(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (plan.n_splits > 1 && launch_fwd_merge(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  return EXATTN_OK;
 }
 
 extern "C" const char* exattn_status_string(int status) {

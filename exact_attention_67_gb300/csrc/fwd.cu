@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
                     float* __restrict__ lse_out, int N_max, int H, int BH, int n_pairs, int window,
-                    float scale_log2, SeqView seq, unsigned* err) {
+                    float scale_log2, SeqView seq, KvSplit kv, unsigned* err) {
   using C = FwdCfg<D>;
   using E = Elem<T>;
   using Bars = FwdBars<C::STAGES>;
@@ -83,8 +83,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   EXATTN_TRACE_INIT();
 
-  // Heaviest work first: under the causal mask the last query pairs see the most keys.
-  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
+  // Heaviest work first: under the causal mask the last query pairs see the
+  // most keys.  blockIdx = (pair, key split, batch*head).
+  const int per_pair = BH * kv.n_splits;
+  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / per_pair;
+  const int split = static_cast<int>(blockIdx.x) % per_pair / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int hh = bh % H, bb = bh / H;  // head and batch index
   const int q0 = pair * 2 * C::BM;
@@ -93,22 +96,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const SeqRows sr0 = seq_rows(seq, bb, hh, H, N_max);
   const int N = sr0.n, row0 = sr0.start, bt = sr0.b_coord;
   if (q0 >= N) return;
-  // Keys any row of a query tile can see: up to the diagonal (causal) or
-  // window - 1 past its last row (window W > 0: key j visible to query i iff
-  // i - j < W, and also j - i < W without the causal mask), and from the
-  // first row's window start.  Both tiles of the CTA stream key tiles from
-  // the first tile of query tile 0 (kv_lo), tile 1 at most one tile early.
+  // Keys: Nk of them, the queries aligned to the last N (query i at key
+  // position i + off; off = 0 unless a decode-shaped call gave more keys).
+  const int Nk = kv.nk > 0 ? kv.nk : N;
+  const int off = Nk - N;
+  // Keys any row of a query tile can see: up to its diagonal (causal) or
+  // window - 1 past it (window W > 0: key j visible to query i iff
+  // i + off - j < W, and also j - i - off < W without the causal mask), and
+  // from the first row's window start.  Both tiles of the CTA stream key
+  // tiles from the first tile of query tile 0 (kv_lo), tile 1 at most one
+  // tile early, within this CTA's key split.
   auto key_end = [&](int t) {  // exclusive
     const int r0 = q0 + t * C::BM, r1 = min(N, r0 + C::BM);
     if (r0 >= N) return 0;
-    if (CAUSAL) return r1;
-    return window > 0 ? min(N, r1 - 1 + window) : N;
+    if (CAUSAL) return min(Nk, r1 + off);
+    return window > 0 ? min(Nk, r1 - 1 + off + window) : Nk;
   };
-  const int kv_lo = window > 0 ? max(0, q0 - window + 1) / C::BN : 0;
-  // Key tiles visited by query tile t, counted from kv_lo (0 if the tile lies wholly past N).
+  const int split_lo = split * kv.tiles_per_split, split_hi = split_lo + kv.tiles_per_split;
+  const int kv_lo = max(window > 0 ? max(0, q0 + off - window + 1) / C::BN : 0, split_lo);
+  // Key tiles visited by query tile t, counted from kv_lo (0 if none).
   auto tiles_for = [&](int t) {
     const int e = key_end(t);
-    return e == 0 ? 0 : (e + C::BN - 1) / C::BN - kv_lo;
+    return e == 0 ? 0 : max(0, min((e + C::BN - 1) / C::BN, split_hi) - kv_lo);
   };
   const int nkv0 = tiles_for(0), nkv1 = tiles_for(1);
   const int n_iter = max(nkv0, nkv1);
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     float m_ref = -INFINITY;  // reference max, log2 units of the scaled logits
     float l = 0.f;            // running sum of 2^(x - m_ref), fp32 terms (for lse)
     float lb = 0.f;           // the same sum over the bf16-rounded terms the PV MMA uses (for O)
-    bool ok = (t == 0 ? nkv0 : nkv1) > 0;
+    bool ok = true;  // cleared only by a wait that gave up
     for (int j = 0; ok && j < (t == 0 ? nkv0 : nkv1); ++j) {
       if (!(ok = mbar_wait(&bars->s_full[t], j & 1, wc))) break;
       if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 0);
@@ -314,14 +323,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int tr0 = q0 + t * C::BM;  // first row of this query tile
       // Some key of this tile is hidden from some row of the query tile: past
       // the diagonal, past N, or outside a row's window.
-      const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > tr0) || (kv0 + C::BN > N) ||
-                             (window > 0 && (kv0 < tr0 + C::BM - window ||
-                                             (!CAUSAL && kv0 + C::BN - 1 > tr0 + window - 1)));
+      const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > tr0 + off) || (kv0 + C::BN > Nk) ||
+                             (window > 0 && (kv0 < tr0 + off + C::BM - window ||
+                                             (!CAUSAL && kv0 + C::BN - 1 > tr0 + off + window - 1)));
       if (need_mask) {
-        int lim = N - kv0;  // visible columns c: lo <= c < lim
-        if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
-        else if (window > 0) lim = min(lim, row_g + window - kv0);
-        const int lo = window > 0 ? row_g - window + 1 - kv0 : 0;
+        const int pos = row_g + off;  // this row's key position
+        int lim = Nk - kv0;           // visible columns c: lo <= c < lim
+        if (CAUSAL) lim = min(lim, pos - kv0 + 1);
+        else if (window > 0) lim = min(lim, pos + window - kv0);
+        const int lo = window > 0 ? pos - window + 1 - kv0 : 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -406,8 +416,37 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       lb = lb * alpha + (rbs.x + rbs.y);
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && (t == 0 ? nkv0 : nkv1) > 0) ok = mbar_wait(&bars->o_full[t], 0, wc);
-    if (ok && (t == 0 ? nkv0 : nkv1) > 0) {
+    const bool any = (t == 0 ? nkv0 : nkv1) > 0;
+    if (ok && any) ok = mbar_wait(&bars->o_full[t], 0, wc);
+    if (ok && kv.part_o) {
+      // Key split: this split's O (normalised within it) and both
+      // logsumexps in fp32; a row that saw no key here gets O = 0 and -inf.
+      const long long prow = (static_cast<long long>(split) * BH + bh) * kv.nq_pad + row_g;
+      float* po = kv.part_o + prow * D;
+      const float inv_l = lb > 0.f ? 1.f / lb : 0.f;
+      if (any) tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o_r[32];
+        if (any) {
+          tmem_ld32(tO + c * 32, o_r);
+          tmem_wait_ld();
+        }
+        if (row_g < N) {
+          float4* dst = reinterpret_cast<float4*>(po + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = any ? make_float4(__uint_as_float(o_r[4 * v4]) * inv_l, __uint_as_float(o_r[4 * v4 + 1]) * inv_l,
+                                        __uint_as_float(o_r[4 * v4 + 2]) * inv_l,
+                                        __uint_as_float(o_r[4 * v4 + 3]) * inv_l)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (row_g < N) {
+        kv.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        kv.part_lseb[prow] = lb > 0.f ? (m_ref + log2f(lb)) * 0.6931471805599453f : -INFINITY;
+      }
+    } else if (ok && any) {
       tc_fence_after();
       const float inv_l = 1.f / lb;
       T* orow = out + bt * so.b + hh * so.h + static_cast<long long>(row0 + row_g) * so.n;
@@ -443,11 +482,16 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<T, D, CAUSAL>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
+  KvSplit kv = a.kv;
+  if (kv.n_splits < 1) {  // one CTA covers all keys of its query pair
+    kv.n_splits = 1;
+    kv.tiles_per_split = 1 << 30;
+  }
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
-  const long long grid = static_cast<long long>(n_pairs) * a.BH;
+  const long long grid = static_cast<long long>(n_pairs) * kv.n_splits * a.BH;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, a.window,
-      a.scale_log2, a.seq, a.err);
+      a.scale_log2, a.seq, kv, a.err);
   return cudaGetLastError();
 }
 
@@ -459,6 +503,69 @@ static cudaError_t launch_fwd_dt(const FwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   return a.dtype == kF16 ? launch_fwd_dt<__half>(a, stream) : launch_fwd_dt<__nv_bfloat16>(a, stream);
+}
+
+// ---------------------------------------------------------------- split merge
+// O and lse of query row r from the key splits' partials: with the splits'
+// logsumexps L_s (exact sums) and Lb_s (rounded weights), lse = log sum_s
+// exp(L_s) and O = sum_s exp(Lb_s - log sum_s' exp(Lb_s')) O_s -- the same
+// two normalisations the single-CTA forward uses, over all keys.  One warp
+// per row, lane c owns columns c, c + 32, ...
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o,
+                                                         const float* __restrict__ part_lse,
+                                                         const float* __restrict__ part_lseb, int n_splits,
+                                                         int nq_pad, int N, int H, int BH, T* __restrict__ out,
+                                                         Strides so, float* __restrict__ lse_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = static_cast<long long>(blockIdx.x) * 4 + warp;  // (bh, row)
+  if (item >= static_cast<long long>(BH) * N) return;
+  const int bh = static_cast<int>(item / N), row = static_cast<int>(item % N);
+  const int hh = bh % H, bb = bh / H;
+  float mx = -INFINITY, mxb = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) {
+    const long long pr = (static_cast<long long>(s) * BH + bh) * nq_pad + row;
+    mx = fmaxf(mx, part_lse[pr]);
+    mxb = fmaxf(mxb, part_lseb[pr]);
+  }
+  float sum = 0.f, sumb = 0.f;
+  float acc[D / 32];
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
+  for (int s = 0; s < n_splits; ++s) {
+    const long long pr = (static_cast<long long>(s) * BH + bh) * nq_pad + row;
+    const float L = part_lse[pr], Lb = part_lseb[pr];
+    if (L != -INFINITY) sum += expf(L - mx);
+    if (Lb == -INFINITY) continue;
+    const float w = expf(Lb - mxb);
+    sumb += w;
+    const float* po = part_o + pr * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, po[c * 32 + lane], acc[c]);
+  }
+  const float inv = sumb > 0.f ? 1.f / sumb : 0.f;
+  T* orow = out + bb * so.b + hh * so.h + static_cast<long long>(row) * so.n;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    const float v = acc[c] * inv;
+    if constexpr (Elem<T>::kFmt == 1) orow[c * 32 + lane] = __float2bfloat16_rn(v);
+    else orow[c * 32 + lane] = __float2half_rn(v);
+  }
+  if (lane == 0) lse_out[static_cast<long long>(bh) * N + row] = mx + logf(sum);
+}
+
+template <typename T, int D>
+static cudaError_t launch_merge_t(const FwdArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.BH) * a.N;
+  attn_merge_kernel<T, D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+      a.kv.part_o, a.kv.part_lse, a.kv.part_lseb, a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH,
+      static_cast<T*>(a.o), a.so, a.lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_merge(const FwdArgs& a, cudaStream_t stream) {
+  if (a.dtype == kF16) return a.d == 64 ? launch_merge_t<__half, 64>(a, stream) : launch_merge_t<__half, 128>(a, stream);
+  return a.d == 64 ? launch_merge_t<__nv_bfloat16, 64>(a, stream) : launch_merge_t<__nv_bfloat16, 128>(a, stream);
 }
 
 }  // namespace exattn

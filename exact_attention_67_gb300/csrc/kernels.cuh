@@ -50,6 +50,22 @@ __device__ __forceinline__ SeqRows seq_rows(const SeqView& sv, int b, int h, int
   return r;
 }
 
+// Key side of the forward when it differs from the query side: nk keys per
+// problem with the queries aligned to the last nq of them (bottom-right:
+// query i sits at key position i + nk - nq), and the keys split over
+// n_splits CTAs of tiles_per_split 128-key tiles each.  With part_o set,
+// every split writes fp32 partial results that launch_fwd_merge combines:
+//   part_o    [n_splits, B*H, nq_pad, d]  O of the split (normalised within it)
+//   part_lse  [n_splits, B*H, nq_pad]     logsumexp of the split (exact sum)
+//   part_lseb [n_splits, B*H, nq_pad]     logsumexp of the rounded weights
+struct KvSplit {
+  int nk;  // 0: as many keys as queries, no offset
+  int n_splits, tiles_per_split, nq_pad;
+  float* part_o;
+  float* part_lse;
+  float* part_lseb;
+};
+
 struct FwdArgs {
   const CUtensorMap* tm_q;  // 4-D maps (d, N, H, B), box 64 x 128 x 1 x 1, 128-byte swizzle
   const CUtensorMap* tm_k;
@@ -60,6 +76,7 @@ struct FwdArgs {
   int N, H, BH, d, causal, dtype;
   int window;               // 0, or W >= 1: key j visible to query i iff i - j < W (and j - i < W if not causal)
   SeqView seq;              // N is the longest sequence when seq.cu_seqlens is set
+  KvSplit kv;               // decode-shaped problems (kv.nk > 0); zero otherwise
   float scale_log2;         // scale * log2(e)
   unsigned* err;            // device watchdog word
   int device;
@@ -98,6 +115,8 @@ struct BwdArgs {
 
 cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+// Combines the split partials of a forward with a.kv.part_o set into O and lse.
+cudaError_t launch_fwd_merge(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);

@@ -217,6 +217,30 @@ int attn_bwd_varlen(int dtype, const void* q, exattn_strides q_strides, const vo
                     void* stream);
 
 /*
+ * Decode-shaped forward: few queries against many keys (token-by-token
+ * generation, the inference latency goal of "Gemini 3 Flash的注意力内核重写：
+ * 算子融合如何实现亚毫秒级推理", §引言).  Q and O are [B, H, Nq, d], K and V
+ * [B, H, Nk, d] (strided as for the _ex calls), lse fp32 [B, H, Nq].  The
+ * queries are the last Nq positions of the key sequence (bottom-right
+ * alignment): under the causal mask query i sees keys j <= i + Nk - Nq, and
+ * a window counts from that position.  With Nq = Nk this is attn_fwd_ex.
+ * The keys are split over several CTAs per (batch, head) when B*H alone
+ * cannot fill the GPU; each split writes fp32 partial results to the
+ * workspace and a second kernel merges them (the same logsumexp-weighted
+ * combination the online softmax uses inside one CTA).
+ *   attn_fwd_decode_workspace_size -- bytes of workspace for this shape (0
+ *     when no split is needed; then workspace may be NULL); 0 also for an
+ *     invalid shape.
+ *   Errors as attn_fwd_ex; Nq > Nk with the causal mask or a window
+ *   returns EXATTN_ERR_SHAPE (a query would see no key).
+ */
+size_t attn_fwd_decode_workspace_size(int B, int H, int Nq, int Nk, int d);
+int attn_fwd_decode(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                    const void* v, exattn_strides v_strides, void* o, exattn_strides o_strides, float* lse, int B,
+                    int H, int Nq, int Nk, int d, int causal, int window, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device
  * memory: a plugin given only its input and output buffers by a runtime that
  * owns all device memory, or code on a latency-critical path where an

@@ -209,3 +209,29 @@ def test_varlen_validation(lib):
 
     assert bwd(cu=None) == 1
     assert bwd(ws=8) == 6
+
+
+def test_decode_validation(lib):
+    """attn_fwd_decode rejects queries that would see no key and bad sizes
+    before any CUDA call; the workspace is zero when no key split is needed."""
+    from exact_attention_67_gb300._lib import Strides
+    P = [0x10000 * (i + 1) for i in range(8)]
+    d = 128
+
+    def st(H, n):
+        return Strides(H * n * d, n * d, d)
+
+    def dec(B=1, H=2, Nq=4, Nk=8, causal=1, window=0, ws=None, wsb=0):
+        return lib.attn_fwd_decode(0, P[0], st(H, Nq), P[1], st(H, Nk), P[2], st(H, Nk), P[3], st(H, Nq), P[4], B, H,
+                                   Nq, Nk, d, causal, window, 0.125, ws, wsb, None)
+
+    assert dec(Nq=9, Nk=8) == 2                       # causal: query 0 would see no key
+    assert dec(Nq=9, Nk=8, causal=0, window=3) == 2
+    assert dec(Nq=0) == 2 and dec(Nk=0) == 2
+    assert dec(window=-1) == 9
+    assert lib.attn_fwd_decode_workspace_size(1, 2, 4, 8, 80) == 0
+    assert lib.attn_fwd_decode_workspace_size(64, 16, 1, 1024, d) == 0   # enough CTAs without a split
+    ws = lib.attn_fwd_decode_workspace_size(1, 1, 1, 32768, d)
+    assert ws > 0
+    assert dec(B=1, H=1, Nq=1, Nk=32768, ws=None) == 6
+    assert dec(B=1, H=1, Nq=1, Nk=32768, ws=P[5], wsb=ws - 1) == 6
