@@ -509,55 +509,87 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
 // O and lse of query row r from the key splits' partials: with the splits'
 // logsumexps L_s (exact sums) and Lb_s (rounded weights), lse = log sum_s
 // exp(L_s) and O = sum_s exp(Lb_s - log sum_s' exp(Lb_s')) O_s -- the same
-// two normalisations the single-CTA forward uses, over all keys.  One warp
-// per row, lane c owns columns c, c + 32, ...
+// two normalisations the single-CTA forward uses, over all keys.  One
+// 256-thread block per row: the threads share the splits for the two
+// logsumexps, then 256 / d groups of d threads (one column each) share them
+// for O, and the groups' sums are added in shared memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMaxSplits = 512;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o,
-                                                         const float* __restrict__ part_lse,
-                                                         const float* __restrict__ part_lseb, int n_splits,
-                                                         int nq_pad, int N, int H, int BH, T* __restrict__ out,
-                                                         Strides so, float* __restrict__ lse_out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long item = static_cast<long long>(blockIdx.x) * 4 + warp;  // (bh, row)
-  if (item >= static_cast<long long>(BH) * N) return;
-  const int bh = static_cast<int>(item / N), row = static_cast<int>(item % N);
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const float* __restrict__ part_o,
+                                                                   const float* __restrict__ part_lse,
+                                                                   const float* __restrict__ part_lseb, int n_splits,
+                                                                   int nq_pad, int N, int H, int BH,
+                                                                   T* __restrict__ out, Strides so,
+                                                                   float* __restrict__ lse_out) {
+  constexpr int G = kMergeThreads / D;  // split groups for the O sum
+  __shared__ float w_s[kMaxSplits];
+  __shared__ float red[2][kMergeThreads / 32];
+  __shared__ float acc_g[G][D];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bh = static_cast<int>(blockIdx.x) / N, row = static_cast<int>(blockIdx.x) % N;
   const int hh = bh % H, bb = bh / H;
-  float mx = -INFINITY, mxb = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) {
-    const long long pr = (static_cast<long long>(s) * BH + bh) * nq_pad + row;
-    mx = fmaxf(mx, part_lse[pr]);
-    mxb = fmaxf(mxb, part_lseb[pr]);
+  auto at = [&](int s) { return (static_cast<long long>(s) * BH + bh) * nq_pad + row; };
+  auto block_reduce = [&](float a, float b, bool is_max, float& ra, float& rb) {
+    for (int o = 16; o > 0; o >>= 1) {
+      const float xa = __shfl_xor_sync(0xffffffffu, a, o), xb = __shfl_xor_sync(0xffffffffu, b, o);
+      a = is_max ? fmaxf(a, xa) : a + xa;
+      b = is_max ? fmaxf(b, xb) : b + xb;
+    }
+    if (lane == 0) {
+      red[0][warp] = a;
+      red[1][warp] = b;
+    }
+    __syncthreads();
+    ra = red[0][0];
+    rb = red[1][0];
+    for (int w = 1; w < kMergeThreads / 32; ++w) {
+      ra = is_max ? fmaxf(ra, red[0][w]) : ra + red[0][w];
+      rb = is_max ? fmaxf(rb, red[1][w]) : rb + red[1][w];
+    }
+    __syncthreads();
+  };
+  float mx_l = -INFINITY, mxb_l = -INFINITY;
+  for (int s = tid; s < n_splits; s += kMergeThreads) {
+    mx_l = fmaxf(mx_l, part_lse[at(s)]);
+    mxb_l = fmaxf(mxb_l, part_lseb[at(s)]);
   }
-  float sum = 0.f, sumb = 0.f;
-  float acc[D / 32];
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
-  for (int s = 0; s < n_splits; ++s) {
-    const long long pr = (static_cast<long long>(s) * BH + bh) * nq_pad + row;
-    const float L = part_lse[pr], Lb = part_lseb[pr];
-    if (L != -INFINITY) sum += expf(L - mx);
-    if (Lb == -INFINITY) continue;
-    const float w = expf(Lb - mxb);
-    sumb += w;
-    const float* po = part_o + pr * D;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, po[c * 32 + lane], acc[c]);
+  float mx, mxb;
+  block_reduce(mx_l, mxb_l, true, mx, mxb);
+  float sum_l = 0.f, sumb_l = 0.f;
+  for (int s = tid; s < n_splits; s += kMergeThreads) {
+    const float L = part_lse[at(s)], Lb = part_lseb[at(s)];
+    if (L != -INFINITY) sum_l += expf(L - mx);
+    const float w = Lb != -INFINITY ? expf(Lb - mxb) : 0.f;
+    w_s[s] = w;
+    sumb_l += w;
   }
-  const float inv = sumb > 0.f ? 1.f / sumb : 0.f;
-  T* orow = out + bb * so.b + hh * so.h + static_cast<long long>(row) * so.n;
+  float sum, sumb;
+  block_reduce(sum_l, sumb_l, false, sum, sumb);  // its barriers also publish w_s
+  const int g = tid / D, c = tid % D;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int s = g; s < n_splits; s += G) acc = fmaf(w_s[s], part_o[at(s) * D + c], acc);
+  acc_g[g][c] = acc;
+  __syncthreads();
+  if (tid < D) {
+    float v = 0.f;
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    const float v = acc[c] * inv;
-    if constexpr (Elem<T>::kFmt == 1) orow[c * 32 + lane] = __float2bfloat16_rn(v);
-    else orow[c * 32 + lane] = __float2half_rn(v);
+    for (int k = 0; k < G; ++k) v += acc_g[k][tid];
+    v *= sumb > 0.f ? 1.f / sumb : 0.f;
+    T* orow = out + bb * so.b + hh * so.h + static_cast<long long>(row) * so.n;
+    if constexpr (Elem<T>::kFmt == 1) orow[tid] = __float2bfloat16_rn(v);
+    else orow[tid] = __float2half_rn(v);
   }
-  if (lane == 0) lse_out[static_cast<long long>(bh) * N + row] = mx + logf(sum);
+  if (tid == 0) lse_out[static_cast<long long>(bh) * N + row] = mx + logf(sum);
 }
 
 template <typename T, int D>
 static cudaError_t launch_merge_t(const FwdArgs& a, cudaStream_t stream) {
+  if (a.kv.n_splits > kMaxSplits) return cudaErrorInvalidValue;
   const long long rows = static_cast<long long>(a.BH) * a.N;
-  attn_merge_kernel<T, D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+  attn_merge_kernel<T, D><<<static_cast<unsigned>(rows), kMergeThreads, 0, stream>>>(
       a.kv.part_o, a.kv.part_lse, a.kv.part_lseb, a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH,
       static_cast<T*>(a.o), a.so, a.lse);
   return cudaGetLastError();
