@@ -389,27 +389,43 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     if (ok) {
       tc_fence_after();
 
+      // Rows leave through shared memory (the K, V tiles are no longer read:
+      // every MMA is done): each thread writes its row, then each warp stores
+      // its 32 rows with coalesced 16-byte lanes (whole rows per instruction)
+      // instead of 32 rows 256 bytes apart per instruction.
+      constexpr int VPR = D / 8;        // 16-byte vectors per row
+      constexpr int RPI = 32 / VPR;     // rows per warp instruction
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t tacc = tmem + lane_bits + (which == 0 ? C::TM_DK : C::TM_DV);
         const float mul = which == 0 ? scale : 1.f;
         const Strides& so = which == 0 ? sdk : sdv;
-        T* dst_row = (which == 0 ? dk : dv) + bt * so.b + hh * so.h + static_cast<long long>(row0 + key) * so.n;
+        uint4* stage = reinterpret_cast<uint4*>(smem + (which == 0 ? C::OFF_K : C::OFF_V)) + warp * 32 * VPR;
+        // The whole row in one round trip to TMEM (the main loop's registers are free now).
+        uint32_t r[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tacc + c * 32, r[c]);
+        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tacc + c * 32, r);
-          tmem_wait_ld();
-          if (key < N) {
-            uint32_t pk[16];
+          uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = E::pack(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = E::pack(__uint_as_float(r[c][2 * e]) * mul, __uint_as_float(r[c][2 * e + 1]) * mul);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-          }
+          for (int v4 = 0; v4 < 4; ++v4)  // vector j of the row at slot j ^ (row % VPR): spreads the banks
+            stage[lane * VPR + ((c * 4 + v4) ^ (lane % VPR))] =
+                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+        __syncwarp();
+        T* base = (which == 0 ? dk : dv) + bt * so.b + hh * so.h;
+#pragma unroll
+        for (int i = 0; i < VPR; ++i) {
+          const int rl = i * RPI + lane / VPR, j = lane % VPR;  // row within the warp, vector within the row
+          const int krow = k0 + warp * 32 + rl;
+          if (krow < N)
+            reinterpret_cast<uint4*>(base + static_cast<long long>(row0 + krow) * so.n)[j] =
+                stage[rl * VPR + (j ^ (rl % VPR))];
         }
       }
     }
