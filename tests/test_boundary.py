@@ -235,3 +235,19 @@ def test_decode_validation(lib):
     assert ws > 0
     assert dec(B=1, H=1, Nq=1, Nk=32768, ws=None) == 6
     assert dec(B=1, H=1, Nq=1, Nk=32768, ws=P[5], wsb=ws - 1) == 6
+
+
+def test_host_path_rejects_bad_tensors():
+    """fwd_bwd_from_host checks its host tensors before any device work."""
+    import torch
+    from exact_attention_67_gb300.host import fwd_bwd_from_host
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fwd_bwd_from_host(q, q, q[:, :1], q)  # shape mismatch
+    with pytest.raises(ValueError):
+        fwd_bwd_from_host(q.float(), q.float(), q.float(), q.float())  # fp32
+    with pytest.raises(ValueError):
+        t = q.transpose(1, 2)
+        fwd_bwd_from_host(t, t, t, t)  # not contiguous
+    with pytest.raises(ValueError):
+        fwd_bwd_from_host(q, q, q, q, out=(q, q, q, q, q))  # lse of the wrong type and shape

@@ -105,3 +105,21 @@ def test_layout_does_not_change_bits():
     res = run_ex(ins, True, w.scale, ["bnhd", "pad", "bnhd", "pad", "bnhd", "pad", "bnhd", "pad"])
     for name, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
         assert torch.equal(res[name], ref.cpu()), name
+
+
+@pytest.mark.parametrize("dtype,groups", [(torch.bfloat16, 2), (torch.float16, 3), (torch.bfloat16, 1)])
+def test_host_path_equals_device_path(dtype, groups):
+    """fwd_bwd_from_host (host tensors in and out, copies overlapped with the
+    kernels in groups of heads) gives the device path's results bit for bit."""
+    import exact_attention_67_gb300 as ex
+    from exact_attention_67_gb300.host import fwd_bwd_from_host
+    w, ins = custom(2, 3, 300, 128, True, seed=61, dtype=dtype)
+    pin = [t.pin_memory() for t in ins]
+    outs = fwd_bwd_from_host(*pin, True, w.scale, groups=groups, device=DEV)
+    torch.cuda.synchronize()
+    q, k, v, do = (t.to(DEV) for t in ins)
+    o, lse = ex.forward(q, k, v, True, w.scale)
+    dq, dk, dv = ex.backward(q, k, v, o, lse, do, True, w.scale)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), outs, (o, lse, dq, dk, dv)):
+        assert torch.equal(a, b.cpu()), name
