@@ -267,7 +267,9 @@ def reference_arm(args, w, rank: int, world: int):
 
 
 def workload_config(w, world: int):
-    return {"workload": f"{w.name} fwd+bwd" if w.bwd else f"{w.name} fwd",
+    # Every step times the forward and the backward, also for a workload whose
+    # published figure is forward-only (its fwd_tflops is that figure).
+    return {"workload": f"{w.name} fwd+bwd",
             "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
             "scale": "1/sqrt(d)", "inputs": "bf16 N(0,1) (Q,K sigma %g), seeded" % w.sigma_qk,
             "l2": "flushed before every step (256 MiB write, outside the timed events)",

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dk, Strides sdk,
-                    T* __restrict__ dv, Strides sdv, int N_max, int H, int BH, int n_ktiles, int window, float scale,
+                    T* __restrict__ dv, Strides sdv, int N_max, int H, int BH, int n_ktiles, int group, int window,
+                    float scale,
                     float scale_log2, SeqView seq, unsigned* err) {
   using C = DkdvCfg<D>;
   using E = Elem<T>;
@@ -124,8 +125,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   EXATTN_TRACE_INIT();
 
   // Under the causal mask the first key tiles meet the most queries: run them first.
-  const int kt = static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const GridPos gp = grid_pos(static_cast<int>(blockIdx.x), BH, n_ktiles, 1, group);
+  const int kt = gp.tile;
+  const int bh = gp.bh;
   const int hh = bh % H, bb = bh / H;  // head and batch index
   const int k0 = kt * C::BM;
   // This batch's rows (a packed variable-length batch may be shorter than the
@@ -461,9 +463,10 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
   const int n_kt = (a.N + C::BM - 1) / C::BM;
+  const int group = l2_group(2ll * a.N * D * static_cast<long long>(sizeof(T)), a.BH);  // Q, dO
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
-      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, a.window, a.scale, a.scale_log2, a.seq, a.err);
+      static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return cudaGetLastError();
 }
 

@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dq, Strides sdq,
-                  int N_max, int H, int BH, int n_pairs, int window, float scale, float scale_log2, SeqView seq,
+                  int N_max, int H, int BH, int n_pairs, int group, int window, float scale, float scale_log2,
+                  SeqView seq,
                   unsigned* err) {
   using C = DqCfg<D>;
   using E = Elem<T>;
@@ -87,8 +88,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   EXATTN_TRACE_INIT();
 
   // Under the causal mask the last query tiles meet the most keys: run them first.
-  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const GridPos gp = grid_pos(static_cast<int>(blockIdx.x), BH, n_pairs, 1, group);
+  const int pair = n_pairs - 1 - gp.tile;
+  const int bh = gp.bh;
   const int hh = bh % H, bb = bh / H;  // head and batch index
   const int q0 = pair * 2 * C::BM;
   // This batch's rows (a packed variable-length batch may be shorter than the
@@ -380,9 +382,10 @@ static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  const int group = l2_group(2ll * a.N * D * static_cast<long long>(sizeof(T)), a.BH);  // K, V
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<T*>(a.dq), a.sdq, a.N, a.H,
-      a.BH, n_pairs, a.window, a.scale, a.scale_log2, a.seq, a.err);
+      a.BH, n_pairs, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return cudaGetLastError();
 }
 

@@ -71,7 +71,7 @@ template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
-                    float* __restrict__ lse_out, int N_max, int H, int BH, int n_pairs, int window,
+                    float* __restrict__ lse_out, int N_max, int H, int BH, int n_pairs, int group, int window,
                     float scale_log2, SeqView seq, KvSplit kv, unsigned* err) {
   using C = FwdCfg<D>;
   using E = Elem<T>;
@@ -84,11 +84,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   EXATTN_TRACE_INIT();
 
   // Heaviest work first: under the causal mask the last query pairs see the
-  // most keys.  blockIdx = (pair, key split, batch*head).
-  const int per_pair = BH * kv.n_splits;
-  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / per_pair;
-  const int split = static_cast<int>(blockIdx.x) % per_pair / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // most keys.  blockIdx = (group of heads, pair, key split, head in group).
+  const GridPos gp = grid_pos(static_cast<int>(blockIdx.x), BH, n_pairs, kv.n_splits, group);
+  const int pair = n_pairs - 1 - gp.tile;
+  const int split = gp.sub;
+  const int bh = gp.bh;
   const int hh = bh % H, bb = bh / H;  // head and batch index
   const int q0 = pair * 2 * C::BM;
   // This batch's rows (a packed variable-length batch may be shorter than the
@@ -489,8 +489,15 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   }
   const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long grid = static_cast<long long>(n_pairs) * kv.n_splits * a.BH;
+  // Group heads so their K and V stay in L2 -- except when the key splits read
+  // disjoint key ranges (nothing is re-read across CTAs) or the packed
+  // sequences differ in length (plain heaviest-first order balances them
+  // better; measured).
+  const int group = (kv.n_splits > 1 || a.seq.cu_seqlens)
+                        ? a.BH
+                        : l2_group(2ll * (kv.nk > 0 ? kv.nk : a.N) * D * static_cast<long long>(sizeof(T)), a.BH);
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, a.window,
+      *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, group, a.window,
       a.scale_log2, a.seq, kv, a.err);
   return cudaGetLastError();
 }

@@ -50,6 +50,48 @@ __device__ __forceinline__ SeqRows seq_rows(const SeqView& sv, int b, int h, int
   return r;
 }
 
+// Grid order shared by the attention kernels.  The (batch, head) problems run
+// in groups of `group`, sized on the host (l2_group) so that the operand the
+// CTAs of one problem all re-read -- K and V for the forward and dQ, Q and dO
+// for dK/dV -- stays in L2 for the whole group; within a group the tiles go
+// heaviest first (tile 0 is the caller's heaviest) and problems fastest.
+// With group == BH this is plain (tile, sub, problem) order.
+struct GridPos {
+  int tile, sub, bh;
+};
+
+__device__ __forceinline__ GridPos grid_pos(int block, int BH, int n_tiles, int n_sub, int group) {
+  const long long b = block;
+  const long long per_full = static_cast<long long>(group) * n_tiles * n_sub;
+  const long long full = BH / group;  // complete groups
+  long long g, r;
+  int size;
+  if (b < full * per_full) {
+    g = b / per_full;
+    r = b % per_full;
+    size = group;
+  } else {
+    g = full;
+    r = b - full * per_full;
+    size = BH - static_cast<int>(full) * group;
+  }
+  const long long per_tile = static_cast<long long>(size) * n_sub;
+  GridPos p;
+  p.tile = static_cast<int>(r / per_tile);
+  p.sub = static_cast<int>(r % per_tile / size);
+  p.bh = static_cast<int>(g * group + r % size);
+  return p;
+}
+
+// Problems per group for grid_pos: as many as keep their re-read operands
+// (bytes_per_problem each) within half of the 129 MB L2, at least one.
+constexpr long long kL2GroupBytes = 64ll << 20;
+inline int l2_group(long long bytes_per_problem, int BH) {
+  long long g = bytes_per_problem > 0 ? kL2GroupBytes / bytes_per_problem : BH;
+  if (g > BH) g = BH;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
 // Key side of the forward when it differs from the query side: nk keys per
 // problem with the queries aligned to the last nq of them (bottom-right:
 // query i sits at key position i + nk - nq), and the keys split over
