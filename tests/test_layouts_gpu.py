@@ -123,3 +123,24 @@ def test_host_path_equals_device_path(dtype, groups):
     torch.cuda.synchronize()
     for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), outs, (o, lse, dq, dk, dv)):
         assert torch.equal(a, b.cpu()), name
+
+
+def test_host_step_replays_current_inputs():
+    """HostStep (the host path as one CUDA graph) matches the device path bit
+    for bit, and a replay picks up new contents of the pinned inputs."""
+    import exact_attention_67_gb300 as ex
+    w, ins = custom(1, 5, 700, 64, True, seed=71)
+    w2, ins2 = custom(1, 5, 700, 64, True, seed=72)
+    pin = [t.pin_memory() for t in ins]
+    step = ex.HostStep(*pin, True, w.scale, groups=3, streams=2, device=DEV)
+    for src in (ins, ins2):
+        for p_, t in zip(pin, src):
+            p_.copy_(t)
+        outs = step()
+        torch.cuda.synchronize()
+        q, k, v, do = (t.to(DEV) for t in src)
+        o, lse = ex.forward(q, k, v, True, w.scale)
+        dq, dk, dv = ex.backward(q, k, v, o, lse, do, True, w.scale)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), outs, (o, lse, dq, dk, dv)):
+            assert torch.equal(a, b.cpu()), name
