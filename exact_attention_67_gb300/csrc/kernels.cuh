@@ -60,7 +60,7 @@ struct GridPos {
   int tile, sub, bh;
 };
 
-__device__ __forceinline__ GridPos grid_pos(int block, int BH, int n_tiles, int n_sub, int group) {
+__host__ __device__ __forceinline__ GridPos grid_pos(int block, int BH, int n_tiles, int n_sub, int group) {
   const long long b = block;
   const long long per_full = static_cast<long long>(group) * n_tiles * n_sub;
   const long long full = BH / group;  // complete groups
