@@ -236,11 +236,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       }
     }
     // The two issuers take turns, one block of MMAs (dQ_t, then the next S_t,
-    // dP_t) each.  A block is handed over a few MMAs before its end, so the
-    // next issuer is already queueing while the tensor core finishes it: the
-    // queue in front of the tensor core is shallow, and an empty queue costs
-    // the pipeline's fill latency at every block.
-    constexpr int kTail = D == 128 ? 2 : 1;  // product k-steps left when the turn passes
+    // dP_t) each, and pass the turn once their block is issued: the other
+    // issuer, already past its own waits, queues its block right behind.
+    // (Passing the turn a few MMAs before the end of the block measured
+    // slower: two k-steps early cost dQ 7 % at d = 128, one 4 % at d = 64.)
     for (int it = 0; ok && it < n_iter; ++it) {
       const int s = it % C::STAGES;
       const uint32_t turn_par = static_cast<uint32_t>(it & 1) ^ (t == 0 ? 1u : 0u);
@@ -266,9 +265,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         if (more) {
           // S_t, dP_t of the next step overwrite the dS_t the dQ MMA just read:
           // the tensor core runs one thread's MMAs in issue order.
-          issue_products(t, s1, 0, D / 16 - kTail);
+          issue_products(t, s1, 0, D / 16);
           mbar_arrive(&bars->turn[t ^ 1]);
-          issue_products(t, s1, D / 16 - kTail, D / 16);
           mma_commit(&bars->s_full[t]);
         } else {
           mbar_arrive(&bars->turn[t ^ 1]);
