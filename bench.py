@@ -400,19 +400,20 @@ def main():
     # ---------------------------------------------------------------- e2e
     e2e = None
     if not args.no_e2e:
-        from exact_attention_67_gb300.host import HostStep
         pin = [t.pin_memory() for t in (q_h, k_h, v_h, do_h)]
         outs_h = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv))
         n_e2e = max(3, min(steps, 20))
-        e2e_groups, e2e_streams = min(4, w.B * w.H), 2
-        # Host in, host out: the library's host path, captured once as a CUDA
-        # graph (outside the timed region).  Every step copies each group's
-        # inputs in and its results out on two copy streams while the kernels
-        # of other groups (two compute streams) or later stages run.
-        host_step = HostStep(*pin, causal, scale, groups=e2e_groups, streams=e2e_streams, device=dev, out=outs_h)
+        e2e_groups = min(4, w.B * w.H)
+        ws_host = torch.empty(ex.attn_fwd_bwd_host_workspace_size(w.B, w.H, w.N, w.d, causal), dtype=torch.uint8,
+                              device=dev)
+        s_in, s_out, s_two = (torch.cuda.Stream(device=dev) for _ in range(3))
 
         def e2e_step():
-            host_step()
+            # Host in, host out through the C ABI: attn_fwd_bwd_host copies each
+            # group's inputs in on s_in and its results out on s_out while the
+            # kernels of other groups (on `stream` and s_two) or later stages run.
+            ex.attn_fwd_bwd_host(*pin, *outs_h, causal, scale, ws_host, groups=e2e_groups, stream=stream,
+                                 copy_in_stream=s_in, copy_out_stream=s_out, stream2=s_two)
 
         for _ in range(2):
             e2e_step()
@@ -430,9 +431,9 @@ def main():
         d2h = sum(t.numel() * t.element_size() for t in outs_h)
         e2e = {"value": job_tflops(3.5 * F, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n_e2e,
-               "path": "HostStep (fwd_bwd_from_host captured as one CUDA graph): pinned host inputs -> "
+               "path": "C ABI attn_fwd_bwd_host with host buffers, called every step: pinned host inputs -> "
                        "device, forward and backward kernels, device -> pinned host outputs, copies overlapped "
-                       f"with the kernels ({e2e_groups} groups of heads on {e2e_streams} compute streams)"}
+                       f"with the kernels ({e2e_groups} groups of heads on 2 compute streams)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

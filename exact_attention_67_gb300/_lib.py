@@ -25,6 +25,7 @@ STATUS_NAMES = {
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen",
            "attn_fwd_decode_workspace_size", "attn_fwd_decode", "attn_bwd_noalloc",
+           "attn_fwd_bwd_host_workspace_size", "attn_fwd_bwd_host",
            "exattn_status_string",
            "exattn_device_error", "exattn_watchdog_selftest", "exattn_version")
 
@@ -90,6 +91,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_fwd_decode.restype = i
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_noalloc.restype = i
+        lib.attn_fwd_bwd_host_workspace_size.argtypes = [i, i, i, i, i]
+        lib.attn_fwd_bwd_host_workspace_size.restype = sz
+        lib.attn_fwd_bwd_host.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, i, vp, vp, vp,
+                                          vp]
+        lib.attn_fwd_bwd_host.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.attn_bwd_workspace_size.restype = sz
         lib.exattn_status_string.argtypes = [i]
@@ -343,6 +349,41 @@ def attn_bwd_dq(q, k, v, dO, lse, D, dq, causal: bool, scale: float, stream=None
     _check_rows(D, (B, H, N), "D")
     _check(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq), B, H, N, d,
                               int(bool(causal)), float(scale), _stream(stream)))
+
+
+def attn_fwd_bwd_host_workspace_size(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    """C ``attn_fwd_bwd_host_workspace_size`` (bytes; 0 for invalid sizes)."""
+    return int(load().attn_fwd_bwd_host_workspace_size(int(B), int(H), int(N), int(d), int(bool(causal))))
+
+
+def attn_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, causal: bool, scale: float, workspace, groups: int = 4,
+                      stream=None, copy_in_stream=None, copy_out_stream=None, stream2=None) -> None:
+    """C ``attn_fwd_bwd_host``: q, k, v, dO and the outputs o, lse, dq, dk, dv
+    are contiguous HOST tensors (pinned, for the copies to overlap the
+    kernels); ``workspace`` is a device tensor of at least
+    ``attn_fwd_bwd_host_workspace_size`` bytes.  Streams: torch streams, or
+    None (``stream``: the current stream; the others: run on ``stream``)."""
+    if q.dim() != 4:
+        raise ValueError(f"q must be [B, H, N, d], got {tuple(q.shape)}")
+    B, H, N, d = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if tuple(t.shape) != (B, H, N, d) or t.dtype != q.dtype or t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{n}: expected a contiguous host tensor like q")
+    if tuple(lse.shape) != (B, H, N) or lse.dtype != torch.float32 or lse.device.type != "cpu" or \
+            not lse.is_contiguous():
+        raise ValueError("lse: expected a contiguous fp32 host tensor [B, H, N]")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q: bf16 or f16")
+    dtype = EXATTN_DTYPE_F16 if q.dtype == torch.float16 else EXATTN_DTYPE_BF16
+    ws_bytes = workspace.numel() * workspace.element_size()
+
+    def side(s):
+        return None if s is None else _stream(s)
+
+    _check(load().attn_fwd_bwd_host(dtype, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(lse), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                                    _ptr(workspace), ws_bytes, int(groups), _stream(stream), side(copy_in_stream),
+                                    side(copy_out_stream), side(stream2)))
 
 
 def device_error() -> int:

@@ -265,6 +265,43 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
                      float scale, void* stream);
 
+/*
+ * Forward and backward on host-resident tensors: attn_fwd followed by the
+ * backward (the fused forward of "Gemini 3 Flash的注意力内核重写：算子融合如何
+ * 实现亚毫秒级推理", §1 内核融合策略, and its recomputing backward, §4), with
+ * the host <-> device copies inside the call.  The (batch, head) problems
+ * run in `groups` groups: each group's Q, K, V then dO are copied in on
+ * copy_in_stream while earlier groups compute; its O and lse are copied out
+ * on copy_out_stream while its backward runs, dK and dV while its dQ is
+ * computed, then dQ.  Odd-numbered groups compute on stream2 when it is
+ * given (the kernels of small groups then share the GPU), the others on
+ * `stream`.
+ *   dtype : EXATTN_DTYPE_BF16 or EXATTN_DTYPE_F16.
+ *   q, k, v, dO : HOST memory, contiguous [B, H, N, d] of dtype; o, dq, dk,
+ *     dv likewise (outputs), lse fp32 [B, H, N] (output).  Use page-locked
+ *     (pinned) memory: copies from pageable memory are not asynchronous and
+ *     do not overlap the kernels.
+ *   workspace : device memory of at least attn_fwd_bwd_host_workspace_size
+ *     bytes, 16-byte aligned, owned by the caller; it holds the device copies
+ *     of all nine tensors and the backward's row terms.
+ *   groups : >= 1 (clamped to B*H).
+ *   stream : the call's work is ordered after the work already queued on
+ *     it, and everything queued on it afterwards runs after the call's work
+ *     (the copies included): synchronise it before reading the outputs.
+ *     copy_in_stream, copy_out_stream, stream2 : other streams of the same
+ *     device, or NULL (that role then runs on `stream`, without overlap).
+ * Asynchronous; allocates no device memory; creates and destroys a few CUDA
+ * events per call (their last uses complete with the call's work).
+ * Validation and errors as attn_bwd (workspace: EXATTN_ERR_WORKSPACE;
+ * groups < 1: EXATTN_ERR_VALUE).  An error returned after the first copy
+ * was queued leaves the outputs undefined.
+ */
+size_t attn_fwd_bwd_host_workspace_size(int B, int H, int N, int d, int causal);
+int attn_fwd_bwd_host(int dtype, const void* q, const void* k, const void* v, const void* dO, void* o, float* lse,
+                      void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                      void* workspace, size_t workspace_bytes, int groups, void* stream, void* copy_in_stream,
+                      void* copy_out_stream, void* stream2);
+
 /* Human-readable text of an exattn_status (static storage, never NULL). */
 const char* exattn_status_string(int status);
 

@@ -251,3 +251,25 @@ def test_host_path_rejects_bad_tensors():
         fwd_bwd_from_host(t, t, t, t)  # not contiguous
     with pytest.raises(ValueError):
         fwd_bwd_from_host(q, q, q, q, out=(q, q, q, q, q))  # lse of the wrong type and shape
+
+
+def test_host_entry_point_validates_before_any_copy():
+    """attn_fwd_bwd_host rejects bad arguments before touching the device."""
+    import torch
+    from exact_attention_67_gb300 import _lib
+    lib = _lib.load()
+    assert lib.attn_fwd_bwd_host_workspace_size(1, 2, 128, 96, 1) == 0     # d not 64 or 128
+    need = lib.attn_fwd_bwd_host_workspace_size(1, 2, 128, 64, 1)
+    assert need >= 8 * 2 * 128 * 64 * 2 + 2 * 2 * 128 * 4
+    x = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 128)
+    small = torch.zeros(16, dtype=torch.uint8)  # far too small (and not device memory: never touched)
+    p = [t.data_ptr() for t in (x, x, x, x, x, lse, x, x, x)]
+    W, V, N_ = _lib.EXATTN_OK + 6, _lib.EXATTN_OK + 9, _lib.EXATTN_OK + 1
+    assert lib.attn_fwd_bwd_host(0, *p, 1, 2, 128, 64, 1, 0.125, small.data_ptr(), 16, 2, None, None, None, None) == W
+    assert lib.attn_fwd_bwd_host(0, *p, 1, 2, 128, 64, 1, 0.125, small.data_ptr(), need, 0, None, None, None, None) == V
+    assert lib.attn_fwd_bwd_host(0, *p, 1, 2, 128, 64, 1, -1.0, small.data_ptr(), need, 2, None, None, None, None) == V
+    assert lib.attn_fwd_bwd_host(0, None, *p[1:], 1, 2, 128, 64, 1, 0.125, small.data_ptr(), need, 2, None, None,
+                                 None, None) == N_
+    assert lib.attn_fwd_bwd_host(7, *p, 1, 2, 128, 64, 1, 0.125, small.data_ptr(), need, 2, None, None, None,
+                                 None) == _lib.EXATTN_OK + 4
