@@ -177,8 +177,11 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KTILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_4d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, row0 + k0, hh, bt, pol_keep);
-        tma_load_4d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, row0 + k0, hh, bt, pol_keep);
+        // K, V of this key tile are read by this CTA alone.
+        tma_load_4d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::KCHUNK, c * 64, row0 + k0, hh, bt,
+                    l2_policy_evict_first());
+        tma_load_4d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::KCHUNK, c * 64, row0 + k0, hh, bt,
+                    l2_policy_evict_first());
       }
     }
     // Row terms of the next step are fetched into registers one step ahead, so
