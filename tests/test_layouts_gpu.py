@@ -144,3 +144,31 @@ def test_host_step_replays_current_inputs():
         torch.cuda.synchronize()
         for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), outs, (o, lse, dq, dk, dv)):
             assert torch.equal(a, b.cpu()), name
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,groups,side,dtype", [
+    (3, 1, 77, 64, True, 5, False, torch.bfloat16),     # more groups than problems; every role on one stream
+    (1, 1, 300, 128, False, 1, True, torch.bfloat16),   # one problem, ragged N
+    (2, 3, 129, 64, True, 4, True, torch.float16),      # f16 backward in one call per group
+])
+def test_host_entry_point_edge_cases(B, H, N, d, causal, groups, side, dtype):
+    """attn_fwd_bwd_host (the C ABI's host-buffer call) on awkward shapes and
+    stream set-ups gives the device path's results bit for bit."""
+    import exact_attention_67_gb300 as ex
+    w, ins = custom(B, H, N, d, causal, seed=81 + N, dtype=dtype)
+    pin = [t.pin_memory() for t in ins]
+    outs = (torch.empty_like(ins[0]).pin_memory(), torch.empty(B, H, N).pin_memory(),
+            torch.empty_like(ins[0]).pin_memory(), torch.empty_like(ins[0]).pin_memory(),
+            torch.empty_like(ins[0]).pin_memory())
+    ws = torch.empty(ex.attn_fwd_bwd_host_workspace_size(B, H, N, d, causal), dtype=torch.uint8, device=DEV)
+    streams = [torch.cuda.Stream(device=DEV) for _ in range(3)] if side else [None, None, None]
+    ex.attn_fwd_bwd_host(*pin, outs[0], outs[1], outs[2], outs[3], outs[4], causal, w.scale, ws, groups=groups,
+                         copy_in_stream=streams[0], copy_out_stream=streams[1], stream2=streams[2])
+    torch.cuda.synchronize()
+    q, k, v, do = (t.to(DEV) for t in ins)
+    o, lse = ex.forward(q, k, v, causal, w.scale)
+    dq, dk, dv = ex.backward(q, k, v, o, lse, do, causal, w.scale)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), outs, (o, lse, dq, dk, dv)):
+        assert torch.equal(a, b.cpu()), name
+    assert ex.device_error() == 0
