@@ -620,4 +620,4 @@ extern "C" int exattn_watchdog_selftest(unsigned timeout_us, void* stream) {
   return cudaGetLastError() == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
-extern "C" int exattn_version(void) { return 100; }
+extern "C" int exattn_version(void) { return 200; }  // 0.2.0: attn_fwd_bwd_host
