@@ -273,3 +273,24 @@ def test_host_entry_point_validates_before_any_copy():
                                  None, None) == N_
     assert lib.attn_fwd_bwd_host(7, *p, 1, 2, 128, 64, 1, 0.125, small.data_ptr(), need, 2, None, None, None,
                                  None) == _lib.EXATTN_OK + 4
+
+
+def test_binding_argument_counts_match_the_header():
+    """Every C prototype in include/exattn.h has as many parameters as the
+    ctypes binding declares for it (a mismatch would pass wrong arguments)."""
+    import re
+    from exact_attention_67_gb300 import _lib
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "include", "exattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)  # drop comments
+    protos = re.findall(r"^\s*(?:const\s+)?[\w]+\s*\**\s*(\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.M | re.S)
+    lib = _lib.load()
+    seen = 0
+    for name, params in protos:
+        if name not in _lib.EXPORTS:
+            continue
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(getattr(lib, name).argtypes) == n, name
+        seen += 1
+    assert seen == len(_lib.EXPORTS)
