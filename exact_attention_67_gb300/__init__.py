@@ -22,7 +22,7 @@ __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preproce
            "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward",
            "backward", "forward_varlen", "backward_varlen", "attn_fwd_decode", "attn_fwd_decode_workspace_size",
            "forward_decode", "fwd_bwd_from_host", "HostStep", "attn_fwd_bwd_host",
-           "attn_fwd_bwd_host_workspace_size", "device_error",
+           "attn_fwd_bwd_host_workspace_size", "attention", "flash_attn_func", "device_error",
            "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
 
 
@@ -109,3 +109,6 @@ def forward_decode(q, k, v, causal: bool = False, scale: float | None = None, st
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     attn_fwd_decode(q, k, v, o, lse, causal, s, ws, stream, window)
     return o, lse
+
+
+from .autograd import attention, flash_attn_func  # noqa: E402  (uses forward/backward above)
