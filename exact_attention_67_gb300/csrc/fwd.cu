@@ -8,7 +8,7 @@
 // wholly above the causal diagonal are never visited ("提示词再优也救不了的性能
 // 黑洞…", 第一章, causal=True skips the upper triangle).
 //
-// GB300 mapping (one CTA per SM, 320 threads):
+// GB300 mapping (one CTA per SM; 320 threads, 384 with bf16 inputs):
 //   * the CTA owns two 128-row query tiles (256 rows) of one (batch, head);
 //     they share one stream of 128-row K/V tiles;
 //   * warp 8 issues TMA loads: both Q tiles once, then K_j and V_j into
@@ -21,10 +21,16 @@
 //     128 scores, updates the running max, rescales the running sum and the
 //     TMEM O row when the max has grown by more than 2^8 (the reference max
 //     is otherwise kept; the final normalisation by the same reference makes
-//     the result identical), writes P = 2^(s*scale*log2e - m) in the input
-//     type (bf16 or f16) over the S columns, and hands the tile back to the
-//     MMA warp.  While one warpgroup does its softmax the tensor core works
-//     on the other tile.
+//     the result identical), writes P = 2^(s*scale*log2e - m) as f16 over
+//     the S columns, and hands the tile back to the MMA warp.  While one
+//     warpgroup does its softmax the tensor core works on the other tile.
+//   * P V runs in f16 whatever the input type: P rounded to f16 (11
+//     significant bits) errs 8x less than bf16 (8 bits), which keeps O within
+//     its error bound on rows dominated by a few keys.  The MMA takes both
+//     operands in one type, so for bf16 inputs warps 10-11 convert each V
+//     tile to f16 in shared memory, in place, between its TMA landing and its
+//     first P V (exact for 2^-14 <= |v| <= 65504 and for 0; smaller
+//     magnitudes are carried with an absolute error below 2^-25).
 //   * epilogue: O_t / l rounded to the input type, lse = (m + log2 l) ln 2;
 //     l for O sums the rounded P that the PV MMA used.
 // TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
@@ -51,11 +57,20 @@ struct FwdCfg {
   static constexpr uint32_t TM_S = 0, TM_O = 256, TM_COLS = 512;
 };
 
+// Threads of the forward CTA: 8 softmax warps, the TMA warp and the MMA warp,
+// plus two warps that convert V tiles to f16 when the inputs are bf16.
+template <typename T>
+struct FwdThreads {
+  static constexpr bool kConvertV = Elem<T>::kFmt != Elem<__half>::kFmt;
+  static constexpr int value = kConvertV ? 384 : 320;
+};
+
 template <int STAGES>
 struct FwdBars {
   uint64_t q_full[2];
   uint64_t k_full[STAGES], k_empty[STAGES];
   uint64_t v_full[STAGES], v_empty[STAGES];
+  uint64_t v_conv[STAGES];  // V tile converted to f16 (bf16 inputs only)
   uint64_t s_full[2];  // S_t ready (also: every earlier MMA of the CTA done)
   uint64_t p_full[2];  // P_t written to TMEM by the 128 softmax threads
   uint64_t o_full[2];  // last P_t V_j of tile t done
@@ -67,14 +82,21 @@ struct FwdBars {
 // Rescale threshold for the running max, in log2 units: P stays below 2^8.
 constexpr float kRescaleThreshold = 8.0f;
 
+// bf16 pair -> f16 pair, round to nearest even (exact in the f16 normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 template <typename T, int D, bool CAUSAL>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+__global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
                     float* __restrict__ lse_out, int N_max, int H, int BH, int n_pairs, int group, int window,
                     float scale_log2, SeqView seq, KvSplit kv, unsigned* err) {
   using C = FwdCfg<D>;
   using E = Elem<T>;
+  using PE = Elem<__half>;  // P and the converted V: the P V product runs in f16
+  constexpr bool kConvertV = FwdThreads<T>::kConvertV;
   using Bars = FwdBars<C::STAGES>;
   static_assert(sizeof(Bars) <= 512, "barrier block too large");
   extern __shared__ uint8_t smem_raw[];
@@ -135,6 +157,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->v_conv[s], 64);
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -200,7 +223,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // The whole warp runs this loop (waits and descriptor arithmetic stay
     // warp-uniform); the elected lane issues the tcgen05 instructions.
     constexpr uint32_t idesc_s = idesc_f16kind(E::kFmt, 128, C::BN, 0, 0);  // Q, K both K-major
-    constexpr uint32_t idesc_o = idesc_f16kind(E::kFmt, 128, D, 0, 1);      // P from TMEM, V MN-major
+    constexpr uint32_t idesc_o = idesc_f16kind(PE::kFmt, 128, D, 0, 1);     // f16 P from TMEM, f16 V MN-major
     const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
     const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::CHUNK_BYTES, 1024);
@@ -257,7 +280,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (!(ok = wait_all(&bars->p_full[t], j & 1))) continue;
         if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 0);
         if (!v_ready) {
-          if (!(ok = wait_all(&bars->v_full[s], ph))) continue;
+          if (!(ok = wait_all(kConvertV ? &bars->v_conv[s] : &bars->v_full[s], ph))) continue;
           v_ready = true;
         }
         if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 1);
@@ -297,6 +320,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     __syncwarp();
     if (lane == 0) mbar_wait_drain(&bars->mma_done, 0, err);
     __syncwarp();
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ V to f16 (bf16 inputs)
+    // 64 threads convert each landed V tile in place (the layout is the same
+    // for both 16-bit types), then make their generic-proxy stores visible to
+    // the tensor core's async-proxy reads before arriving.
+    if constexpr (kConvertV) {
+      constexpr int NVEC = C::TILE_BYTES / 16;  // 16-byte vectors per tile
+      constexpr int PER = NVEC / 64, BATCH = 8;
+      static_assert(PER % BATCH == 0, "conversion batches must divide the tile");
+      const int ct = (warp - 10) * 32 + lane;
+      for (int j = 0; j < n_iter; ++j) {
+        const int s = j % C::STAGES;
+        if (!mbar_wait(&bars->v_full[s], (j / C::STAGES) & 1, wc)) break;
+        uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_V + s * C::TILE_BYTES);
+#pragma unroll 1
+        for (int b0 = 0; b0 < PER; b0 += BATCH) {
+          uint4 x[BATCH];
+#pragma unroll
+          for (int u = 0; u < BATCH; ++u) x[u] = tile[(b0 + u) * 64 + ct];
+#pragma unroll
+          for (int u = 0; u < BATCH; ++u)
+            tile[(b0 + u) * 64 + ct] = make_uint4(bf16x2_to_f16x2(x[u].x), bf16x2_to_f16x2(x[u].y),
+                                                  bf16x2_to_f16x2(x[u].z), bf16x2_to_f16x2(x[u].w));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->v_conv[s]);
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
@@ -308,7 +359,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t tO = tmem + lane_bits + C::TM_O + t * 128;
     float m_ref = -INFINITY;  // reference max, log2 units of the scaled logits
     float l = 0.f;            // running sum of 2^(x - m_ref), fp32 terms (for lse)
-    float lb = 0.f;           // the same sum over the bf16-rounded terms the PV MMA uses (for O)
+    float lb = 0.f;           // the same sum over the f16-rounded terms the PV MMA uses (for O)
     bool ok = true;  // cleared only by a wait that gave up
     for (int j = 0; ok && j < (t == 0 ? nkv0 : nkv1); ++j) {
       if (!(ok = mbar_wait(&bars->s_full[t], j & 1, wc))) break;
@@ -373,7 +424,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // Packed partial sums: short FADD chains, half the instructions.
       float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
-      uint32_t pk[4][16];  // P as bf16 pairs, kept for the rounded sum below
+      uint32_t pk[4][16];  // P as f16 pairs, kept for the rounded sum below
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -381,7 +432,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const float2 y = ffma2(make_float2(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])), sc2, nm2);
           const float2 p = make_float2(ex2(y.x), ex2(y.y));
           rs[e & 1] = fadd2(rs[e & 1], p);
-          pk[c][e] = E::pack(p.x, p.y);
+          pk[c][e] = PE::pack(p.x, p.y);
         }
         tmem_st16(tS + c * 16, pk[c]);  // P_t over the first 64 columns of S_t
       }
@@ -403,7 +454,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tc_fence_before();
       if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 1);
       mbar_arrive(&bars->p_full[t]);
-      // O is normalised by the sum of the bf16-rounded weights the PV MMA
+      // O is normalised by the sum of the f16-rounded weights the PV MMA
       // used: a row dominated by a few keys then keeps an exact convex
       // combination of V rows instead of inheriting their rounding.  Done
       // after the hand-off, off the tensor core's critical path.
@@ -411,7 +462,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) rb[e & 1] = E::add_pair(pk[c][e], rb[e & 1]);
+        for (int e = 0; e < 16; ++e) rb[e & 1] = PE::add_pair(pk[c][e], rb[e & 1]);
       const float2 rbs = fadd2(rb[0], rb[1]);
       lb = lb * alpha + (rbs.x + rbs.y);
     }
@@ -496,7 +547,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const int group = (kv.n_splits > 1 || a.seq.cu_seqlens)
                         ? a.BH
                         : l2_group(2ll * (kv.nk > 0 ? kv.nk : a.N) * D * static_cast<long long>(sizeof(T)), a.BH);
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
+  kern<<<static_cast<unsigned>(grid), FwdThreads<T>::value, C::SMEM_BYTES, stream>>>(
       *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, group, a.window,
       a.scale_log2, a.seq, kv, a.err);
   return cudaGetLastError();

@@ -2,7 +2,8 @@
 on seeded inputs and compare with the fp64 oracle.
 
 Tolerances (fixed for this method; bf16 inputs, fp32 accumulation):
-  O    max |err| <= 1e-2 beyond bf16 output rounding, mean |err| <= 1e-3
+  O    max |err| <= 1e-2, mean |err| <= 1e-3 (raw errors; only elements whose
+       own output rounding can exceed 1e-2 are excused, one by one)
   lse  max |err| <= 1e-3
   dQ, dK, dV  ||err||_F / ||ref||_F <= 2e-2
 """
@@ -56,24 +57,40 @@ def out_bits(t: torch.Tensor) -> int:
 
 def check_fwd(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what="",
               bits: int = 8):
-    """O is bf16 (bits = 8) or f16 (bits = 11), so an exact result rounded to
-    it is already off by up to half an ulp (bf16: 0.0156 for |O| in [4, 8)),
-    and by about a quarter ulp on average (bf16: ~2e-3 for |O| in [1, 2),
-    above the mean bound on its own in a short row).  Both O bounds apply to
-    the error beyond that rounding; the raw errors are reported too."""
+    """The stated bounds on the raw error: O max-abs <= 1e-2 and mean-abs
+    <= 1e-3 over every element, lse max-abs <= 1e-3.
+
+    One exception, for elements where rounding the exact value to the output
+    type alone can exceed the max bound: half an ulp of O_ref above 1e-2
+    (bf16, bits = 8: |O_ref| >= 4, where half an ulp is 0.0156; f16 needs
+    |O_ref| >= 32).  Such an element may err by its half ulp plus 1e-3 (the
+    mean bound) and is listed with its index and both values."""
     assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
     assert np.all(np.isfinite(lse_gpu)), f"{what}: non-finite lse"
     err = np.abs(o_gpu - o_ref)
-    beyond = err - half_ulp(o_ref, bits)
-    beyond_mean = float(np.maximum(beyond, 0.0).mean()) if err.size else 0.0
+    hu = half_ulp(o_ref, bits)
+    roundable = hu > TOL_O_MAX
+    over = err > TOL_O_MAX
+    excused = over & roundable & (err <= hu + TOL_O_MEAN)
+    failing = over & ~excused
     lerr = np.abs(lse_gpu - lse_ref)
-    n_raw = int(np.count_nonzero(err > TOL_O_MAX))
-    info = (f"{what}: O max {err.max():.3e} (beyond output rounding {beyond.max():.3e}; "
-            f"{n_raw} elements > {TOL_O_MAX} raw) mean {err.mean():.3e} (beyond rounding {beyond_mean:.3e}); "
-            f"lse max {lerr.max():.3e}; max|O| {np.abs(o_ref).max():.3f}")
-    assert beyond.max() <= TOL_O_MAX, info
-    assert beyond_mean <= TOL_O_MEAN, info
-    assert lerr.max() <= TOL_LSE_MAX, info
+    mean = float(err.mean()) if err.size else 0.0
+    emax = float(err.max()) if err.size else 0.0
+    small = ~roundable
+    emax_small = float(err[small].max()) if np.any(small) else 0.0
+    info = (f"{what}: O max {emax:.3e} (over |O_ref| with half-ulp <= 1e-2: {emax_small:.3e}) mean {mean:.3e}; "
+            f"lse max {(lerr.max() if lerr.size else 0.0):.3e}; max|O| {(np.abs(o_ref).max() if o_ref.size else 0.0):.3f}; "
+            f"{int(excused.sum())} element(s) excused as output rounding at |O_ref| with half-ulp > 1e-2")
+    for idx in np.argwhere(excused)[:20]:
+        t = tuple(int(x) for x in idx)
+        info += f"\n  excused {t}: O_ref {o_ref[t]:.6f} O_gpu {o_gpu[t]:.6f} err {err[t]:.3e} half-ulp {hu[t]:.3e}"
+    if np.any(failing):
+        t = tuple(int(x) for x in np.argwhere(failing)[0])
+        info += (f"\n  {int(failing.sum())} element(s) over {TOL_O_MAX}, first {t}: O_ref {o_ref[t]:.6f} "
+                 f"O_gpu {o_gpu[t]:.6f} err {err[t]:.3e}")
+    assert not np.any(failing), info
+    assert mean <= TOL_O_MEAN, info
+    assert lerr.size == 0 or lerr.max() <= TOL_LSE_MAX, info
     return info
 
 
