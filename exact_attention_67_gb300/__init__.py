@@ -6,24 +6,30 @@ tile-by-tile recomputation from the stored logsumexp.  The C ABI is in
 ``include/exattn.h``; ``attn_fwd`` / ``attn_bwd`` here are its ctypes binding
 (same names, argument marshalling only) and :func:`forward` /
 :func:`backward` allocate the outputs with PyTorch.
+
+The helpers (forward, backward, their varlen and decode forms, attention)
+also watch the kernels' watchdog without synchronising: each call queues a
+copy of the device's watchdog word into page-locked memory after its
+launches, and the next call raises ExattnError (EXATTN_ERR_TIMEOUT) if a
+completed copy shows that a bounded wait gave up.
 """
 from __future__ import annotations
 
 import math
 
 from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
-                   attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_decode,
-                   attn_fwd_bwd_host, attn_fwd_bwd_host_workspace_size, attn_fwd_decode_workspace_size,
-                   attn_fwd_ex, attn_fwd_varlen, device_error, library_path, load,
-                   status_string, version)
+                   attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_decode, attn_fwd_bwd_host,
+                   attn_fwd_bwd_host_workspace_size, attn_fwd_decode_workspace_size, attn_fwd_ex, attn_fwd_varlen,
+                   device_error, library_path, load, status_string, version, watchdog_check, watchdog_poll)
 from .host import HostStep, fwd_bwd_from_host
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward",
-           "backward", "forward_varlen", "backward_varlen", "attn_fwd_decode", "attn_fwd_decode_workspace_size",
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex",
+           "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward", "backward", "forward_varlen", "backward_varlen", "attn_fwd_decode", "attn_fwd_decode_workspace_size",
            "forward_decode", "fwd_bwd_from_host", "HostStep", "attn_fwd_bwd_host",
            "attn_fwd_bwd_host_workspace_size", "attention", "flash_attn_func", "device_error",
-           "status_string", "version", "load", "library_path", "ExattnError", "EXPORTS"]
+           "watchdog_check", "watchdog_poll", "status_string", "version", "load", "library_path", "ExattnError",
+           "EXPORTS"]
 
 
 def _default_scale(d: int) -> float:
@@ -43,12 +49,14 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
+    watchdog_check(q.device)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if window == 0 and _plain(q, k, v, o):
         attn_fwd(q, k, v, o, lse, causal, s, stream)
     else:
         attn_fwd_ex(q, k, v, o, lse, causal, s, stream, window)
+    watchdog_poll(q.device, stream)
     return o, lse
 
 
@@ -59,6 +67,7 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
+    watchdog_check(q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         nbytes = attn_bwd_workspace_size(B, H, N, d, causal)
@@ -67,6 +76,7 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
         attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
     else:
         attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream, window)
+    watchdog_poll(q.device, stream)
     return dq, dk, dv
 
 
@@ -77,9 +87,11 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, s
     import torch
     total, H, d = q.shape
     s = _default_scale(d) if scale is None else scale
+    watchdog_check(q.device)
     o = torch.empty_like(q)
     lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
     attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, s, stream, window)
+    watchdog_poll(q.device, stream)
     return o, lse
 
 
@@ -89,10 +101,12 @@ def backward_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen: int, causal: bo
     import torch
     total, H, d = q.shape
     s = _default_scale(d) if scale is None else scale
+    watchdog_check(q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = torch.empty(attn_bwd_workspace_size(1, H, total, d, causal), dtype=torch.uint8, device=q.device)
     attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen, causal, s, workspace, stream, window)
+    watchdog_poll(q.device, stream)
     return dq, dk, dv
 
 
@@ -105,9 +119,11 @@ def forward_decode(q, k, v, causal: bool = False, scale: float | None = None, st
     s = _default_scale(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    watchdog_check(q.device)
     nbytes = attn_fwd_decode_workspace_size(B, H, Nq, Nk, d)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     attn_fwd_decode(q, k, v, o, lse, causal, s, ws, stream, window)
+    watchdog_poll(q.device, stream)
     return o, lse
 
 

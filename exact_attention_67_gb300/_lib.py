@@ -27,7 +27,7 @@ EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preproce
            "attn_fwd_decode_workspace_size", "attn_fwd_decode", "attn_bwd_noalloc",
            "attn_fwd_bwd_host_workspace_size", "attn_fwd_bwd_host",
            "exattn_status_string",
-           "exattn_device_error", "exattn_watchdog_selftest", "exattn_version")
+           "exattn_device_error", "exattn_device_error_poll", "exattn_watchdog_selftest", "exattn_version")
 
 EXATTN_DTYPE_BF16 = 0
 EXATTN_DTYPE_F16 = 1
@@ -74,6 +74,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_dkdv.restype = i
         lib.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_dq.restype = i
+        lib.exattn_device_error_poll.argtypes = [vp, vp]
+        lib.exattn_device_error_poll.restype = i
         S = Strides
         lib.attn_fwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, i, i, i, i, i, i, f, vp]
         lib.attn_fwd_ex.restype = i
@@ -127,12 +129,31 @@ def _ptr(t):
     return t.data_ptr()
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The cudaStream_t of a torch stream (or a raw handle); None is the
+    current stream of ``device`` (of the current device if None)."""
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def _device_of(*ts):
+    """The one CUDA device of the given tensors (None entries skipped).  The
+    C ABI runs on the current device, so operands on another device, or on
+    several, are rejected here, before anything is launched."""
+    dev = None
+    for t in ts:
+        if t is None or isinstance(t, int):
+            continue
+        if not t.is_cuda:
+            raise ValueError("all device operands must be CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"operands are on different devices ({dev} and {t.device})")
+    return dev
 
 
 def _shape4(t: torch.Tensor, name: str):
@@ -175,9 +196,11 @@ def attn_fwd_ex(q, k, v, o, lse, causal: bool, scale: float, stream=None, window
             raise ValueError(f"{n} shape/dtype differs from q")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [B, H, N]")
-    _check(load().attn_fwd_ex(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o), views[2][2],
-                              _ptr(lse), B, H, N, d, int(bool(causal)), int(window), float(scale),
-                              _stream(stream)))
+    dev = _device_of(q, k, v, o, lse)
+    with torch.cuda.device(dev):
+        _check(load().attn_fwd_ex(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o), views[2][2],
+                                  _ptr(lse), B, H, N, d, int(bool(causal)), int(window), float(scale),
+                                  _stream(stream, dev)))
 
 
 def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None,
@@ -194,10 +217,12 @@ def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, wor
         raise ValueError("lse must be contiguous float32 [B, H, N]")
     s = [vw[2] for vw in views]
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().attn_bwd_ex(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
-                              _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], B, H, N, d,
-                              int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
-                              _stream(stream)))
+    dev = _device_of(q, k, v, o, dO, lse, dq, dk, dv, workspace)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_ex(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
+                                  _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], B, H, N, d,
+                                  int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
+                                  _stream(stream, dev)))
 
 
 def _packed3(t: torch.Tensor, name: str):
@@ -231,9 +256,11 @@ def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, 
     if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [H, total]")
     B = _cu(cu_seqlens)
-    _check(load().attn_fwd_varlen(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o),
-                                  views[2][2], _ptr(lse), _ptr(cu_seqlens), B, H, int(max_seqlen), total, d,
-                                  int(bool(causal)), int(window), float(scale), _stream(stream)))
+    dev = _device_of(q, k, v, o, lse, cu_seqlens)
+    with torch.cuda.device(dev):
+        _check(load().attn_fwd_varlen(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o),
+                                      views[2][2], _ptr(lse), _ptr(cu_seqlens), B, H, int(max_seqlen), total, d,
+                                      int(bool(causal)), int(window), float(scale), _stream(stream, dev)))
 
 
 def attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen: int, causal: bool, scale: float,
@@ -250,10 +277,12 @@ def attn_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, max_seqlen: int
     B = _cu(cu_seqlens)
     s = [vw[2] for vw in views]
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().attn_bwd_varlen(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
-                                  _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], _ptr(cu_seqlens), B, H,
-                                  int(max_seqlen), total, d, int(bool(causal)), int(window), float(scale),
-                                  _ptr(workspace), ws_bytes, _stream(stream)))
+    dev = _device_of(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, workspace)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_varlen(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o), s[2], _ptr(dO), s[3],
+                                      _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], _ptr(cu_seqlens), B, H,
+                                      int(max_seqlen), total, d, int(bool(causal)), int(window), float(scale),
+                                      _ptr(workspace), ws_bytes, _stream(stream, dev)))
 
 
 def attn_fwd_decode_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
@@ -276,9 +305,11 @@ def attn_fwd_decode(q, k, v, o, lse, causal: bool, scale: float, workspace=None,
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [B, H, Nq]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().attn_fwd_decode(dt, _ptr(q), sq, _ptr(k), sk, _ptr(v), sv, _ptr(o), so, _ptr(lse), B, H, Nq, Nk,
-                                  d, int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
-                                  _stream(stream)))
+    dev = _device_of(q, k, v, o, lse, workspace)
+    with torch.cuda.device(dev):
+        _check(load().attn_fwd_decode(dt, _ptr(q), sq, _ptr(k), sk, _ptr(v), sv, _ptr(o), so, _ptr(lse), B, H, Nq, Nk,
+                                      d, int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
+                                      _stream(stream, dev)))
 
 
 def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
@@ -290,8 +321,10 @@ def attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
             raise ValueError(f"{n} shape {tuple(t.shape)} != q shape {(B, H, N, d)}")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [B, H, N]")
-    _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
-                           float(scale), _stream(stream)))
+    dev = _device_of(q, k, v, o, lse)
+    with torch.cuda.device(dev):
+        _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                               float(scale), _stream(stream, dev)))
 
 
 def attn_bwd_workspace_size(B: int, H: int, N: int, d: int, causal: bool) -> int:
@@ -308,9 +341,11 @@ def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, worksp
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [B, H, N]")
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
-                           _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), ws_bytes,
-                           _stream(stream)))
+    dev = _device_of(q, k, v, o, dO, lse, dq, dk, dv, workspace)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), ws_bytes,
+                               _stream(stream, dev)))
 
 
 def _check_rows(t, shape, name):
@@ -324,7 +359,9 @@ def attn_bwd_preprocess(o, dO, D, stream=None) -> None:
     if _shape4(dO, "dO") != (B, H, N, d):
         raise ValueError("dO shape != o shape")
     _check_rows(D, (B, H, N), "D")
-    _check(load().attn_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d, _stream(stream)))
+    dev = _device_of(o, dO, D)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d, _stream(stream, dev)))
 
 
 def attn_bwd_dkdv(q, k, v, dO, lse, D, dk, dv, causal: bool, scale: float, stream=None) -> None:
@@ -335,8 +372,10 @@ def attn_bwd_dkdv(q, k, v, dO, lse, D, dk, dv, causal: bool, scale: float, strea
             raise ValueError(f"{n} shape != q shape")
     _check_rows(lse, (B, H, N), "lse")
     _check_rows(D, (B, H, N), "D")
-    _check(load().attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dk), _ptr(dv),
-                                B, H, N, d, int(bool(causal)), float(scale), _stream(stream)))
+    dev = _device_of(q, k, v, dO, lse, D, dk, dv)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dk), _ptr(dv),
+                                    B, H, N, d, int(bool(causal)), float(scale), _stream(stream, dev)))
 
 
 def attn_bwd_dq(q, k, v, dO, lse, D, dq, causal: bool, scale: float, stream=None) -> None:
@@ -347,8 +386,10 @@ def attn_bwd_dq(q, k, v, dO, lse, D, dq, causal: bool, scale: float, stream=None
             raise ValueError(f"{n} shape != q shape")
     _check_rows(lse, (B, H, N), "lse")
     _check_rows(D, (B, H, N), "D")
-    _check(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq), B, H, N, d,
-                              int(bool(causal)), float(scale), _stream(stream)))
+    dev = _device_of(q, k, v, dO, lse, D, dq)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq), B, H, N, d,
+                                  int(bool(causal)), float(scale), _stream(stream, dev)))
 
 
 def attn_fwd_bwd_host_workspace_size(B: int, H: int, N: int, d: int, causal: bool) -> int:
@@ -378,22 +419,82 @@ def attn_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, causal: bool, scale: floa
     ws_bytes = workspace.numel() * workspace.element_size()
 
     def side(s):
-        return None if s is None else _stream(s)
+        return None if s is None else _stream(s, dev)
 
-    _check(load().attn_fwd_bwd_host(dtype, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(lse), _ptr(dq),
-                                    _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
-                                    _ptr(workspace), ws_bytes, int(groups), _stream(stream), side(copy_in_stream),
-                                    side(copy_out_stream), side(stream2)))
+    dev = _device_of(workspace)
+    with torch.cuda.device(dev):
+        _check(load().attn_fwd_bwd_host(dtype, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(lse), _ptr(dq),
+                                        _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                                        _ptr(workspace), ws_bytes, int(groups), _stream(stream, dev),
+                                        side(copy_in_stream), side(copy_out_stream), side(stream2)))
 
 
 def device_error() -> int:
-    """Synchronise and read/clear the kernels' watchdog word (0 = clean)."""
-    return int(load().exattn_device_error())
+    """Synchronise and read/clear the kernels' watchdog word of the current
+    device (0 = clean); a pending poll of that word (watchdog_poll) is
+    dropped with it."""
+    rc = int(load().exattn_device_error())
+    w = _watch.get(torch.device("cuda", torch.cuda.current_device()))
+    if w is not None:
+        w.word[0] = 0
+        w.event = None
+    return rc
+
+
+class _Watch:
+    """Per device: a page-locked word that the last poll copies the
+    watchdog word into, and an event recorded after that copy."""
+
+    def __init__(self, dev):
+        self.word = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+        self.event = None
+
+
+_watch: dict = {}
+
+
+def watchdog_check(device) -> None:
+    """Raise ExattnError(EXATTN_ERR_TIMEOUT) if the last completed poll on
+    ``device`` saw a bounded wait give up (then read and clear the word).
+    Never waits: a poll still in flight is checked by a later call."""
+    w = _watch.get(device)
+    if w is None or w.event is None or not w.event.query():
+        return
+    if int(w.word[0]) != 0:
+        w.word[0] = 0
+        w.event = None
+        with torch.cuda.device(device):
+            device_error()  # synchronises, clears the word
+        raise ExattnError(8, "a kernel's bounded internal wait gave up; outputs of the calls since the last "
+                             "check are invalid")
+
+
+def watchdog_poll(device, stream=None) -> None:
+    """Queue a copy of the watchdog word into page-locked memory after the
+    work on ``stream`` (default: the device's current stream); a later
+    watchdog_check reads it once it has landed.  No synchronisation."""
+    w = _watch.get(device)
+    if w is None:
+        w = _watch[device] = _Watch(device)
+    with torch.cuda.device(device):
+        if stream is None:
+            st = torch.cuda.current_stream(device)
+        elif isinstance(stream, int):
+            st = torch.cuda.ExternalStream(stream, device=device)
+        else:
+            st = stream
+        _check(load().exattn_device_error_poll(w.word.data_ptr(), st.cuda_stream))
+        ev = torch.cuda.Event()
+        ev.record(st)
+        w.event = ev
 
 
 def watchdog_selftest(timeout_us: int = 2000, stream=None) -> None:
-    """C ``exattn_watchdog_selftest``: a deliberately unsatisfied bounded wait."""
-    _check(load().exattn_watchdog_selftest(int(timeout_us), _stream(stream)))
+    """C ``exattn_watchdog_selftest``: a deliberately unsatisfied bounded wait
+    on the current device, followed by a watchdog poll (watchdog_poll)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(load().exattn_watchdog_selftest(int(timeout_us), _stream(stream, dev)))
+    watchdog_poll(dev, stream)
 
 
 def version() -> int:

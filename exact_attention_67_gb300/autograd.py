@@ -23,12 +23,16 @@ class _Attention(torch.autograd.Function):
         return o
 
     @staticmethod
+    @torch.autograd.function.once_differentiable
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
         # The library reads dO through its strides (d contiguous, other strides
-        # multiples of 8 elements, nonzero): an expanded or oddly strided
-        # gradient (e.g. from out.sum().backward()) is made contiguous first.
-        if do.stride(-1) != 1 or any(s == 0 or s % 8 for s in do.stride()[:-1]):
+        # multiples of 8 elements, nonzero) from a 16-byte-aligned address: an
+        # expanded, oddly strided or offset gradient (e.g. from
+        # out.sum().backward(), or a slice of a larger buffer) is made
+        # contiguous first.
+        if (do.stride(-1) != 1 or any(s == 0 or s % 8 for s in do.stride()[:-1]) or
+                do.data_ptr() % 16 != 0):
             do = do.contiguous()
         dq, dk, dv = _backward(q, k, v, o, lse, do, ctx.causal, ctx.scale, window=ctx.window)
         return dq, dk, dv, None, None, None

@@ -610,6 +610,18 @@ extern "C" int exattn_device_error(void) {
   return EXATTN_OK;
 }
 
+extern "C" int exattn_device_error_poll(unsigned* host_dst, void* stream) {
+  if (!host_dst) return EXATTN_ERR_NULL;
+  int dev = 0;
+  unsigned* err = nullptr;
+  int rc = device_setup(&dev, &err);
+  if (rc != EXATTN_OK) return rc;
+  return cudaMemcpyAsync(host_dst, err, sizeof(unsigned), cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? EXATTN_OK
+             : EXATTN_ERR_CUDA;
+}
+
 extern "C" int exattn_watchdog_selftest(unsigned timeout_us, void* stream) {
   if (timeout_us < 1 || timeout_us > 1000000) return EXATTN_ERR_VALUE;
   int dev = 0;
@@ -620,4 +632,4 @@ extern "C" int exattn_watchdog_selftest(unsigned timeout_us, void* stream) {
   return cudaGetLastError() == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
-extern "C" int exattn_version(void) { return 200; }  // 0.2.0: attn_fwd_bwd_host
+extern "C" int exattn_version(void) { return 201; }  // 0.2.1: exattn_device_error_poll

@@ -314,6 +314,17 @@ const char* exattn_status_string(int status);
 int exattn_device_error(void);
 
 /*
+ * exattn_device_error_poll -- the watchdog word without synchronising:
+ * queues on `stream` a copy of the current device's word (0 = no wait gave
+ * up; nonzero = exattn_device_error() would return EXATTN_ERR_TIMEOUT) into
+ * *host_dst, after the work already queued there.  The value is valid once
+ * that copy has completed (e.g. an event recorded after it has).  host_dst
+ * should be page-locked, otherwise the copy is synchronous.  Does not clear
+ * the word.  Returns EXATTN_ERR_NULL for a NULL host_dst.
+ */
+int exattn_device_error_poll(unsigned* host_dst, void* stream);
+
+/*
  * exattn_watchdog_selftest -- exercises the failure path of the kernels'
  * bounded waits without any fault: launches one warp that waits on a
  * barrier nothing arrives on, giving up after timeout_us microseconds
