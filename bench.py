@@ -12,18 +12,24 @@ Prints ONE JSON line (rank 0).
 Timing: inputs resident in HBM; L2 is flushed (a 256 MiB write) before every
 step, outside the timed events; each kernel is bracketed by CUDA events on
 the launching stream; the step time is the sum of its kernels' event times.
+After the K timed steps a repeat phase of at least 200 ms of device time
+gives per-kernel and per-step medians (the "median" object); nvidia-smi
+clocks are sampled across both.
 TFLOPS use the algorithmic FLOP model 4*B*H*N^2*d (halved when causal) for
 the forward and 2.5x that for the backward.
 
 Under torchrun (N > 1) every rank runs its own copy of the workload (heads
 are independent: weak scaling, no data-path collective); the reported value
-is the FLOPs of all ranks over the slowest rank's time.
+is the FLOPs of all ranks over the slowest rank's time.  --gpus N > 1 outside
+torchrun relaunches this script under torchrun with N ranks; a --gpus that
+differs from WORLD_SIZE is refused.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import platform
 import statistics
@@ -141,7 +147,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, label: str = "timed region"):
         if self.proc is None or not self.path:
             return None
         rows = []
@@ -162,7 +168,7 @@ class ClockSampler:
         if not rows:
             return None
         inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        window = "timed region"
+        window = label
         if not inside:  # timed region shorter than the sampling period: nearest samples
             inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:3]
             window = "nearest samples to a short timed region"
@@ -275,9 +281,46 @@ def workload_config(w, world: int):
             "parallelism": "replicas" if world == 1 else f"replicas x{world} (independent heads per rank)"}
 
 
+# ------------------------------------------------------------------ launch
+def relaunch_under_torchrun(args) -> int:
+    """--gpus N > 1 outside torchrun: run this script as N ranks on this node
+    (one per GPU) and return their exit status.  Every rank must come up: a
+    replicas run never quietly measures fewer GPUs than asked."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
+def check_world(args):
+    """Exit status for a --gpus / WORLD_SIZE mismatch (None when consistent)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if "WORLD_SIZE" in os.environ and world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU "
+              f"(torchrun --nproc-per-node {args.gpus}) or pass --gpus {world}", file=sys.stderr)
+        return 2
+    return None
+
+
+def kernel_stats(ms_lists):
+    """Per kernel: mean and median of its per-step event times (ms)."""
+    return [(statistics.fmean(v), statistics.median(v)) for v in ms_lists]
+
+
 # ------------------------------------------------------------------ our arm
 def main():
     args = parse_args()
+    if args.gpus < 1:
+        print("bench.py: --gpus must be >= 1", file=sys.stderr)
+        return 2
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return relaunch_under_torchrun(args)
+    bad = check_world(args)
+    if bad is not None:
+        return bad
     from exact_attention_67_gb300.synth import WORKLOADS
     w = WORKLOADS[args.config]
     rank = int(os.environ.get("RANK", "0"))
@@ -294,6 +337,10 @@ def main():
     from exact_attention_67_gb300 import build as exbuild
     from exact_attention_67_gb300.synth import make_inputs
 
+    if not torch.cuda.is_available() or torch.cuda.device_count() <= local:
+        print(f"bench.py: rank {rank} needs CUDA device {local}; {torch.cuda.device_count()} visible",
+              file=sys.stderr)
+        return 1
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -309,13 +356,17 @@ def main():
     q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    Dws = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    Dws = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     causal, scale = w.causal, w.scale
     stream = torch.cuda.current_stream()
-
+    F = w.flops_fwd()
     kernels = ["attn_fwd_kernel", "bwd_rowdot_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+    # algorithmic FLOPs per launch: fwd = 2 GEMMs (QK^T, PV); dK/dV = 4 (S, dP, dV, dK);
+    # dQ = 1 (dQ; its S/dP recomputation is not counted); row dots: bytes only.
+    alg = {"attn_fwd_kernel": F, "bwd_dkdv_kernel": 2.0 * F, "bwd_dq_kernel": 0.5 * F}
+    nbytes = {"bwd_rowdot_kernel": 2 * 2 * w.B * w.H * w.N * w.d + 4 * w.B * w.H * w.N}
 
     def step(evs):
         evs[0].record(stream)
@@ -331,40 +382,55 @@ def main():
     def new_events(n):
         return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
 
-    for evs in new_events(max(3, args.warmup)):
-        flush.zero_()
-        step(evs)
+    def run_steps(n):
+        """n steps, L2 flushed before each (outside its events); per-kernel ms lists."""
+        evs = new_events(n)
+        for i in range(n):
+            flush.zero_()
+            step(evs[i])
+        return evs
+
+    def per_kernel_ms(evs):
+        return [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(4)]
+
+    evw = run_steps(max(3, args.warmup))
     torch.cuda.synchronize()
     if ex.device_error() != 0:
         raise RuntimeError("kernel watchdog fired during warm-up")
+    step_est = sum(statistics.median(x) for x in per_kernel_ms(evw))
 
     sampler = ClockSampler(local, enabled=not args.no_clocks)
     time.sleep(0.3 if not args.no_clocks else 0.0)
-    ev = new_events(args.steps)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()
-        step(ev[i])
+    ev = run_steps(args.steps)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
+    # Repeat phase for order statistics and a clock record over >= 200 ms of
+    # device time, whatever --steps is: the per-kernel medians reported
+    # beside the K-step means.
+    n_rep = max(50, int(math.ceil(200.0 / max(step_est, 1e-3))))
+    ev_rep = run_steps(n_rep)
+    torch.cuda.synchronize()
+    t_wall2 = time.time()
     sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    clocks = sampler.summary(t_wall0, t_wall2, "timed steps and the repeat phase after them")
     if ex.device_error() != 0:
         raise RuntimeError("kernel watchdog fired during the timed region")
 
-    per_kernel = [0.0] * 4
-    for evs in ev:
-        for j in range(4):
-            per_kernel[j] += evs[j].elapsed_time(evs[j + 1])
+    timed = per_kernel_ms(ev)
+    per_kernel = [sum(x) for x in timed]
     reduced = max_over_ranks([sum(per_kernel)] + per_kernel, dev)
     total_ms, per_kernel = reduced[0], reduced[1:]
+    rep = per_kernel_ms(ev_rep)
+    rep_steps = [sum(rep[j][i] for j in range(4)) for i in range(n_rep)]
+    med = max_over_ranks([statistics.median(rep_steps)] + [statistics.median(x) for x in rep], dev)
+    med_step, med_kernel = med[0], med[1:]
 
-    F = w.flops_fwd()
     steps = args.steps
     t_fwd = per_kernel[0] / steps
     t_bwd = sum(per_kernel[1:]) / steps
@@ -372,20 +438,15 @@ def main():
     fwd_tflops = F / t_fwd / 1e9
     bwd_tflops = 2.5 * F / t_bwd / 1e9
     peak = peaks["bf16_tflops"]
-    # algorithmic FLOPs per launch: fwd = 2 GEMMs (QK^T, PV); dK/dV = 4 (S, dP, dV, dK);
-    # dQ = 1 (dQ; its S/dP recomputation is not counted); row dots: bytes only.
-    alg = {"attn_fwd_kernel": F, "bwd_rowdot_kernel": 0.0, "bwd_dkdv_kernel": 2.0 * F,
-           "bwd_dq_kernel": 0.5 * F}
     rows = []
-    for name, ms in zip(kernels, per_kernel):
+    for j, (name, ms) in enumerate(zip(kernels, per_kernel)):
         per = ms / steps
-        r = {"kernel": name, "ms": per, "share": ms / total_ms}
-        if alg[name] > 0:
+        r = {"kernel": name, "ms": per, "median_ms": med_kernel[j], "share": ms / total_ms}
+        if name in alg:
             r["tflops"] = alg[name] / per / 1e9
             r["frac_of_peak"] = r["tflops"] / peak
         else:
-            nbytes = 2 * 2 * w.B * w.H * w.N * w.d + 4 * w.B * w.H * w.N
-            r["gbs"] = nbytes / per / 1e6
+            r["gbs"] = nbytes[name] / per / 1e6
             r["frac_of_hbm"] = r["gbs"] / peaks["hbm_gbs"] if peaks["hbm_gbs"] else None
         rows.append(r)
     dom = max(range(4), key=lambda j: per_kernel[j])
@@ -394,7 +455,11 @@ def main():
     roofline = {"bound": "tensor", "kernel": dname, "achieved": rows[dom].get("tflops"), "peak": peak,
                 "unit": "TFLOP/s", "frac": rows[dom].get("frac_of_peak"), "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-                "algorithmic_flops_per_launch": alg[dname]}
+                "algorithmic_flops_per_launch": alg.get(dname)}
+    median = {"ms_per_step": med_step, "value": job_tflops(3.5 * F, world, med_step),
+              "fwd_tflops": F / med_kernel[0] / 1e9, "bwd_tflops": 2.5 * F / sum(med_kernel[1:]) / 1e9,
+              "steps": n_rep, "device_ms": sum(rep_steps),
+              "note": "medians over a repeat phase run right after the timed steps (same L2 flush per step)"}
 
     # ---------------------------------------------------------------- e2e
     e2e = None
@@ -449,7 +514,7 @@ def main():
             "config": workload_config(w, world),
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "fwd_pct_peak": 100.0 * fwd_tflops / peak, "fwd_bwd_pct_peak": 100.0 * value / world / peak,
-            "kernels": rows, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "median": median, "kernels": rows, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 4 * steps, "clocks": clocks,
             "gpu": torch.cuda.get_device_name(dev)}
     print(json.dumps(line), flush=True)
