@@ -33,7 +33,7 @@
 //     magnitudes are carried with an absolute error below 2^-25).
 //   * epilogue: O_t / l rounded to the input type, lse = (m + log2 l) ln 2;
 //     l for O sums the rounded P that the PV MMA used.
-// TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
+// TMEM: FwdCfg (S, P, O of each tile).
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -54,7 +54,15 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES > 120 * 1024, "one CTA per SM: it holds all 512 TMEM columns");
   static constexpr int THREADS = 320;
-  static constexpr uint32_t TM_S = 0, TM_O = 256, TM_COLS = 512;
+  // TMEM.  d = 128: S_t at 128 t with P_t written over its first 64
+  // columns, O_t at 256 + 128 t.  d = 64: S_t at 128 t, P_t in its own
+  // columns 256 + 64 t, O_t at 384 + 64 t -- P apart from S lets the next
+  // key tile's S_t be computed while the softmax still works on this one.
+  static constexpr bool EARLY_S = D == 64;
+  static constexpr uint32_t TM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t tm_p(int t) { return EARLY_S ? 256u + 64u * t : 128u * t; }
+  __host__ __device__ static constexpr uint32_t tm_o(int t) { return EARLY_S ? 384u + 64u * t : 256u + 128u * t; }
 };
 
 // Threads of the forward CTA: 8 softmax warps, the TMA warp and the MMA warp,
@@ -72,7 +80,9 @@ struct FwdBars {
   uint64_t v_full[STAGES], v_empty[STAGES];
   uint64_t v_conv[STAGES];  // V tile converted to f16 (bf16 inputs only)
   uint64_t s_full[2];  // S_t ready (also: every earlier MMA of the CTA done)
+  uint64_t s_free[2];  // d = 64: the softmax threads of tile t have loaded S_t
   uint64_t p_full[2];  // P_t written to TMEM by the 128 softmax threads
+  uint64_t pv_done[2];  // d = 64: P_t V_j complete (P_t and O_t free)
   uint64_t o_full[2];  // last P_t V_j of tile t done
   uint64_t mma_done;   // every MMA of the CTA done (teardown)
   uint32_t tmem_base;
@@ -148,7 +158,9 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->q_full[t], 1);
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->s_free[t], 128);
       mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_full[t], 1);
     }
     mbar_init(&bars->mma_done, 1);
@@ -234,14 +246,14 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + C::TM_S + t * 128, a + off, b + off, idesc_s, kk > 0);
+        mma_ss(tmem + C::tm_s(t), a + off, b + off, idesc_s, kk > 0);
       }
     };
     auto issue_pv = [&](int t, int stage, bool acc) {
       const uint64_t b = v_desc + stage * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < C::BN / 16; ++kk)
-        mma_ts(tmem + C::TM_O + t * 128, tmem + C::TM_S + t * 128 + kk * 8, b + ((kk * 16 * 128) >> 4), idesc_o,
+        mma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, b + ((kk * 16 * 128) >> 4), idesc_o,
                (acc || kk > 0) ? 1u : 0u);
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -267,52 +279,102 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       }
       __syncwarp();
     }
-    for (int j = 0; ok && j < n_iter; ++j) {
-      const int s = j % C::STAGES;
-      const uint32_t ph = (j / C::STAGES) & 1;
-      const int s1 = (j + 1) % C::STAGES;
-      const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
-      bool v_ready = false, k_ready = false;
+    if constexpr (C::EARLY_S) {
+      // Per key step j: the next scores S_t(j+1) as soon as tile t's softmax
+      // has loaded S_t(j) (its P goes to separate columns), then P_t V_j.
+      for (int j = 0; ok && j < n_iter; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        const int s1 = (j + 1) % C::STAGES;
+        const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+        bool k_ready = false, v_ready = false;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int nkv_t = t == 0 ? nkv0 : nkv1;
-        if (!ok || j >= nkv_t) continue;
-        if (!(ok = wait_all(&bars->p_full[t], j & 1))) continue;
-        if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 0);
-        if (!v_ready) {
-          if (!(ok = wait_all(kConvertV ? &bars->v_conv[s] : &bars->v_full[s], ph))) continue;
-          v_ready = true;
-        }
-        if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 1);
-        tc_fence_after();
-        if (elect_one()) {
-          issue_pv(t, s, j > 0);
-          // V_j is free once the last tile's P V_j is done; releasing it here,
-          // inside the block, keeps the block boundary free of commits.
-          if (t == 1 || nkv1 <= j) mma_commit(&bars->v_empty[s]);
-        }
-        __syncwarp();
-        if (j + 1 < nkv_t) {
+        for (int t = 0; t < 2; ++t) {
+          const int nkv_t = t == 0 ? nkv0 : nkv1;
+          if (!ok || j + 1 >= nkv_t) continue;
+          if (!(ok = wait_all(&bars->s_free[t], j & 1))) continue;
           if (!k_ready) {
             if (!(ok = wait_all(&bars->k_full[s1], ph1))) continue;
             k_ready = true;
-            tc_fence_after();
           }
-          if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 2);
+          tc_fence_after();
           if (elect_one()) {
             issue_s(t, s1);
             mma_commit(&bars->s_full[t]);
           }
           __syncwarp();
-          if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 3);
-        } else {
-          if (elect_one()) mma_commit(&bars->o_full[t]);
+        }
+        if (k_ready) {
+          if (elect_one()) mma_commit(&bars->k_empty[s1]);
+          __syncwarp();
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nkv_t = t == 0 ? nkv0 : nkv1;
+          if (!ok || j >= nkv_t) continue;
+          if (!(ok = wait_all(&bars->p_full[t], j & 1))) continue;
+          if (!v_ready) {
+            if (!(ok = wait_all(kConvertV ? &bars->v_conv[s] : &bars->v_full[s], ph))) continue;
+            v_ready = true;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(t, s, j > 0);
+            mma_commit(&bars->pv_done[t]);
+            if (t == 1 || nkv1 <= j) mma_commit(&bars->v_empty[s]);
+            if (j + 1 == nkv_t) mma_commit(&bars->o_full[t]);
+          }
           __syncwarp();
         }
       }
-      if (k_ready) {
-        if (elect_one()) mma_commit(&bars->k_empty[s1]);
-        __syncwarp();
+    } else {
+      for (int j = 0; ok && j < n_iter; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        const int s1 = (j + 1) % C::STAGES;
+        const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+        bool v_ready = false, k_ready = false;
+  #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nkv_t = t == 0 ? nkv0 : nkv1;
+          if (!ok || j >= nkv_t) continue;
+          if (!(ok = wait_all(&bars->p_full[t], j & 1))) continue;
+          if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 0);
+          if (!v_ready) {
+            if (!(ok = wait_all(kConvertV ? &bars->v_conv[s] : &bars->v_full[s], ph))) continue;
+            v_ready = true;
+          }
+          if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 1);
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(t, s, j > 0);
+            // V_j is free once the last tile's P V_j is done; releasing it here,
+            // inside the block, keeps the block boundary free of commits.
+            if (t == 1 || nkv1 <= j) mma_commit(&bars->v_empty[s]);
+          }
+          __syncwarp();
+          if (j + 1 < nkv_t) {
+            if (!k_ready) {
+              if (!(ok = wait_all(&bars->k_full[s1], ph1))) continue;
+              k_ready = true;
+              tc_fence_after();
+            }
+            if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 2);
+            if (elect_one()) {
+              issue_s(t, s1);
+              mma_commit(&bars->s_full[t]);
+            }
+            __syncwarp();
+            if (lane == 0) EXATTN_TRACE_POINT(1, j, 4 * t + 3);
+          } else {
+            if (elect_one()) mma_commit(&bars->o_full[t]);
+            __syncwarp();
+          }
+        }
+        if (k_ready) {
+          if (elect_one()) mma_commit(&bars->k_empty[s1]);
+          __syncwarp();
+        }
       }
     }
     // Nothing may still read shared memory or write TMEM once the CTA tears down.
@@ -355,8 +417,9 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     const int row = wq * 32 + lane;          // query row within the tile == TMEM lane
     const int row_g = q0 + t * C::BM + row;  // query row within the head
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + C::TM_S + t * 128;
-    const uint32_t tO = tmem + lane_bits + C::TM_O + t * 128;
+    const uint32_t tS = tmem + lane_bits + C::tm_s(t);
+    const uint32_t tP = tmem + lane_bits + C::tm_p(t);
+    const uint32_t tO = tmem + lane_bits + C::tm_o(t);
     float m_ref = -INFINITY;  // reference max, log2 units of the scaled logits
     float l = 0.f;            // running sum of 2^(x - m_ref), fp32 terms (for lse)
     float lb = 0.f;           // the same sum over the f16-rounded terms the PV MMA uses (for O)
@@ -369,6 +432,14 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
       tmem_wait_ld();
+      if constexpr (C::EARLY_S) {
+        // S_t is in registers: the MMA warp may compute the next one over it.
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[t]);
+        // P_t(j-1) V_{j-1} must be done before P_t and O_t are touched again.
+        if (j > 0 && !(ok = mbar_wait(&bars->pv_done[t], (j - 1) & 1, wc))) break;
+        tc_fence_after();
+      }
 
       const int kv0 = (kv_lo + j) * C::BN;
       const int tr0 = q0 + t * C::BM;  // first row of this query tile
@@ -434,12 +505,13 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
           rs[e & 1] = fadd2(rs[e & 1], p);
           pk[c][e] = PE::pack(p.x, p.y);
         }
-        tmem_st16(tS + c * 16, pk[c]);  // P_t over the first 64 columns of S_t
+        tmem_st16(tP + c * 16, pk[c]);  // P_t (d = 128: over the first 64 columns of S_t)
       }
       const float2 r = fadd2(rs[0], rs[1]);
       l = l * alpha + (r.x + r.y);
       if (rescale_warp) {
-        // S_t(j) ready implies P_t(j-1) V_{j-1} has completed: the O row is stable.
+        // P_t(j-1) V_{j-1} has completed (d = 128: S_t(j) is issued after it;
+        // d = 64: pv_done waited above): the O row is stable.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o_r[32];
