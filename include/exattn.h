@@ -255,7 +255,10 @@ int attn_fwd_decode(int dtype, const void* q, exattn_strides q_strides, const vo
  *   The array occupies 16 MiB of device memory on every GPU that loads the
  *   library, until the library is unloaded.  The first call on each device
  *   looks up the array's device address (a runtime query, no allocation);
- *   make that first call before any stream capture.  Every call shares the
+ *   make that first call before any stream capture.  The address stays
+ *   valid for the life of the process's context on that device: after a
+ *   cudaDeviceReset (or a primary-context teardown) this library must not
+ *   be used again in that process.  Every call shares the
  *   array and it keeps the last call's contents (nothing in it needs to start
  *   at zero: each call writes every D_i before reading it), so calls whose
  *   executions overlap on the GPU (e.g. on two streams) race and must be
