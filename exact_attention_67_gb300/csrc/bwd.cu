@@ -11,8 +11,9 @@
 //   1. bwd_rowdot_kernel: D_i = sum_c dO_ic O_ic (bandwidth bound).
 //   2. bwd_dkdv_kernel: one CTA per 128-key tile; streams 64-query tiles of
 //      Q and dO (TMA ring); per tile the tensor core computes S^T = K Q_i^T
-//      and dP^T = V dO_i^T into TMEM, a warpgroup (thread = key row) turns them
-//      into P^T and dS^T (input type, written back over S^T and dP^T), and the
+//      and dP^T = V dO_i^T into TMEM, a warpgroup (thread = key row; two at
+//      d = 64, each on half the query columns) turns them into P^T and dS^T
+//      (input type, written back over S^T and dP^T), and the
 //      tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
 //      S^T/dP^T are double buffered so the next tile's products overlap the
 //      current elementwise work.
@@ -89,7 +90,25 @@ struct DkdvCfg {
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 2 * BR * 4;
   // At least 120 KB so that only one CTA (which holds all 512 TMEM columns) fits on an SM.
   static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
-  static constexpr int THREADS = 192;  // warps 0-3 elementwise, 4 producer, 5 MMA
+  // Elementwise warps: EW_GROUPS groups of four, one warp per TMEM lane
+  // quarter in each group, group g taking query columns 64 g / EW_GROUPS
+  // onwards of the step.  At d = 64 a step's MMA chain is half as long as at
+  // d = 128 while the softmax work is the same, so two groups halve the
+  // hand-off latency that bounds it; at d = 128 the chain hides one group's
+  // latency and the second costs registers.  Then the producer warp, then the
+  // MMA warp.
+  static constexpr int EW_GROUPS = D == 64 ? 2 : 1;
+  static constexpr int EW_WARPS = 4 * EW_GROUPS;
+  static constexpr int PRODUCER_WARP = EW_WARPS, MMA_WARP = EW_WARPS + 1;
+  static constexpr int THREADS = 32 * (EW_WARPS + 2);
+  // P^T (dS^T) of query chunk ch (32 queries, 16 packed columns) is written
+  // from column P_STRIDE ch of S^T (dP^T): with one group a warp owns all of
+  // S^T and packs the chunks side by side; with two, each chunk stays inside
+  // its own 32 columns, which the other group may not have loaded yet.
+  static constexpr int P_STRIDE = EW_GROUPS == 1 ? 16 : 32;
+  // Columns of dK / dV read per TMEM round trip in the epilogue (registers
+  // for the whole row only with one group).
+  static constexpr int EPI_COLS = EW_GROUPS == 1 ? D : 64;
   static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_BUF = 256, TM_COLS = 512;  // buffer b: S^T at +128b, dP^T at +128b+64
 };
 
@@ -152,14 +171,14 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->p_full[b], 32 * C::EW_WARPS);
     }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == C::MMA_WARP) {
     tmem_alloc(&bars->tmem_base, C::TM_COLS);
     tmem_relinquish();
   }
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, err};
 
-  if (warp == 4) {
+  if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_keep = l2_policy_evict_last();  // Q, dO are re-read by every key tile of the head
     if (lane == 0) {
@@ -234,7 +253,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         mbar_wait_drain(&bars->st_full[it % C::STAGES], (it / C::STAGES) & 1, err);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     // Whole-warp loop, elected lane issues (see elect_one()).
     constexpr uint32_t idesc_s = idesc_f16kind(E::kFmt, 128, C::BR, 0, 0);  // K (or V) x Q^T (or dO^T): K-major
@@ -296,10 +315,12 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         const uint64_t qa = q_mn + s * kQTileDesc, da = do_mn + s * kQTileDesc;
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {
-          // dV += P^T dO_i ; dK += dS^T Q_i  (operands over the first 32 columns of S^T / dP^T)
+          // dV += P^T dO_i ; dK += dS^T Q_i.  Queries 16 kk .. 16 kk + 15 of
+          // P^T (dS^T) sit at column P_STRIDE (kk / 2) + 8 (kk % 2) of S^T (dP^T).
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_BUF + b * 128 + kk * 8, da + ((kk * 16 * 128) >> 4), idesc_acc, acc);
-          mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + kk * 8, qa + ((kk * 16 * 128) >> 4), idesc_acc,
+          const uint32_t col = (kk >> 1) * C::P_STRIDE + (kk & 1) * 8;
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_BUF + b * 128 + col, da + ((kk * 16 * 128) >> 4), idesc_acc, acc);
+          mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + col, qa + ((kk * 16 * 128) >> 4), idesc_acc,
                  acc);
         }
         if (it + 1 == nq) {
@@ -319,9 +340,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise (thread = key row)
-    const int row = warp * 32 + lane;
+    // Warp w takes TMEM lane quarter w % 4 and the 32-column chunks
+    // NC (w / 4) .. NC (w / 4) + NC - 1 of the step's 64 query columns.
+    constexpr int NC = 2 / C::EW_GROUPS;
+    const int wq = warp & 3, group = C::EW_GROUPS == 1 ? 0 : warp >> 2;
+    const int row = wq * 32 + lane;
     const int key = k0 + row;
-    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
     bool ok = true;
     for (int it = 0; ok && it < nq; ++it) {
       const int s = it % C::STAGES, b = it & 1;
@@ -332,12 +357,18 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 1);
       tc_fence_after();
       const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tb, sr[0]);
-      tmem_ld32(tb + 32, sr[1]);
-      tmem_ld32(tb + 64, dr[0]);
-      tmem_ld32(tb + 96, dr[1]);
+      uint32_t sr[NC][32], dr[NC][32];
+#pragma unroll
+      for (int g = 0; g < NC; ++g) {
+        tmem_ld32(tb + 32 * (group * NC + g), sr[g]);
+        tmem_ld32(tb + 64 + 32 * (group * NC + g), dr[g]);
+      }
       tmem_wait_ld();
+#pragma unroll
+      for (int g = 0; g < NC; ++g) {
+        tmem_reg_fence(sr[g]);
+        tmem_reg_fence(dr[g]);
+      }
       if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 2);
       const float* st_lse2 = stat + s * 2 * C::BR;
       const float* st_D = st_lse2 + C::BR;
@@ -353,10 +384,12 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         const int c_lo = (CAUSAL ? key : (window > 0 ? key - window + 1 : -C::BR)) - qi0;
         const int c_hi = (window > 0 ? key + window - 1 : qi0 + C::BR) - qi0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int g = 0; g < NC; ++g)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (h * 32 + e < c_lo || h * 32 + e > c_hi) sr[h][e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 32; ++e) {
+            const int c = 32 * (group * NC + g) + e;
+            if (c < c_lo || c > c_hi) sr[g][e] = __float_as_uint(-INFINITY);
+          }
       }
       // Column statistics come from shared memory as float4 broadcasts: four
       // columns per load keeps the shared-memory pipe free for the TMA and
@@ -364,34 +397,38 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       const float4* st_lse4 = reinterpret_cast<const float4*>(st_lse2);
       const float4* st_D4 = reinterpret_cast<const float4*>(st_D);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int g = 0; g < NC; ++g) {
+        const int ch = group * NC + g;  // chunk of 32 query columns
         uint32_t pk[16], dk_[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 L4 = st_lse4[h * 8 + q4], D4 = st_D4[h * 8 + q4];
+          const float4 L4 = st_lse4[ch * 8 + q4], D4 = st_D4[ch * 8 + q4];
           const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};  // -lse2, -D
           float pv[4], dsv[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const int cl = 4 * q4 + w;  // column within this half
-            pv[w] = ex2(fmaf(__uint_as_float(sr[h][cl]), scale_log2, Lv[w]));
-            dsv[w] = pv[w] * (__uint_as_float(dr[h][cl]) + Dv[w]);
+            const int cl = 4 * q4 + w;  // column within the chunk
+            pv[w] = ex2(fmaf(__uint_as_float(sr[g][cl]), scale_log2, Lv[w]));
+            dsv[w] = pv[w] * (__uint_as_float(dr[g][cl]) + Dv[w]);
           }
           pk[2 * q4] = E::pack(pv[0], pv[1]);
           pk[2 * q4 + 1] = E::pack(pv[2], pv[3]);
           dk_[2 * q4] = E::pack(dsv[0], dsv[1]);
           dk_[2 * q4 + 1] = E::pack(dsv[2], dsv[3]);
         }
-        tmem_st16(tb + h * 16, pk);         // P^T over S^T
-        tmem_st16(tb + 64 + h * 16, dk_);   // dS^T over dP^T
+        // P^T of queries 32 ch .. 32 ch + 31 at columns P_STRIDE ch onwards,
+        // dS^T 64 columns further.
+        tmem_st16(tb + ch * C::P_STRIDE, pk);
+        tmem_st16(tb + 64 + ch * C::P_STRIDE, dk_);
       }
       tmem_wait_st();
       if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 3);
       tc_fence_before();
       mbar_arrive(&bars->p_full[b]);
     }
-    if (ok) ok = mbar_wait(&bars->acc_done, 0, wc);
-    if (ok) {
+    // The first four warps write dK and dV.
+    if (ok && group == 0) ok = mbar_wait(&bars->acc_done, 0, wc);
+    if (ok && group == 0) {
       tc_fence_after();
 
       // Rows leave through shared memory (the K, V tiles are no longer read:
@@ -406,21 +443,28 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         const float mul = which == 0 ? scale : 1.f;
         const Strides& so = which == 0 ? sdk : sdv;
         uint4* stage = reinterpret_cast<uint4*>(smem + (which == 0 ? C::OFF_K : C::OFF_V)) + warp * 32 * VPR;
-        // The whole row in one round trip to TMEM (the main loop's registers are free now).
-        uint32_t r[D / 32][32];
+        // The row in round trips of EPI_COLS columns to TMEM.
+        constexpr int RT = C::EPI_COLS / 32;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tacc + c * 32, r[c]);
-        tmem_wait_ld();
+        for (int c0 = 0; c0 < D / 32; c0 += RT) {
+          uint32_t r[RT][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t pk[16];
+          for (int cc = 0; cc < RT; ++cc) tmem_ld32(tacc + (c0 + cc) * 32, r[cc]);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = E::pack(__uint_as_float(r[c][2 * e]) * mul, __uint_as_float(r[c][2 * e + 1]) * mul);
+          for (int cc = 0; cc < RT; ++cc) tmem_reg_fence(r[cc]);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)  // vector j of the row at slot j ^ (row % VPR): spreads the banks
-            stage[lane * VPR + ((c * 4 + v4) ^ (lane % VPR))] =
-                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int cc = 0; cc < RT; ++cc) {
+            const int c = c0 + cc;
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = E::pack(__uint_as_float(r[cc][2 * e]) * mul, __uint_as_float(r[cc][2 * e + 1]) * mul);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)  // vector j of the row at slot j ^ (row % VPR): spreads the banks
+              stage[lane * VPR + ((c * 4 + v4) ^ (lane % VPR))] =
+                  make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
         }
         __syncwarp();
         T* base = (which == 0 ? dk : dv) + bt * so.b + hh * so.h;
@@ -439,7 +483,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, C::TM_COLS);
+  if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TM_COLS);
 }
 
 // ---------------------------------------------------------------- launch
@@ -466,7 +510,11 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
   if (e != cudaSuccess) return e;
   const int n_kt = (a.N + C::BM - 1) / C::BM;
-  const int group = l2_group(2ll * a.N * D * static_cast<long long>(sizeof(T)), a.BH);  // Q, dO
+  // Q, dO of a group's problems stay in a quarter of L2: every key-tile CTA
+  // of a problem re-reads them over the group's waves (B4 H32 N4096 d64:
+  // 1.323 ms with half of L2, 1.280 ms with a quarter; B1 H16 N8192 and B1 H8
+  // N16384 d128 unchanged within 0.5 %).
+  const int group = l2_group(2ll * a.N * D * static_cast<long long>(sizeof(T)), a.BH, kL2GroupBytes / 2);
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
       static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, group, a.window, a.scale, a.scale_log2, a.seq, a.err);

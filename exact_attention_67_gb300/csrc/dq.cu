@@ -306,6 +306,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tmem_ld32(tbase + C::TM_DP, dr[0]);
       tmem_ld32(tbase + C::TM_DP + 32, dr[1]);
       tmem_wait_ld();
+      tmem_reg_fence(sr[0]);
+      tmem_reg_fence(sr[1]);
+      tmem_reg_fence(dr[0]);
+      tmem_reg_fence(dr[1]);
       const int kj0 = (kv_lo + it) * C::BN;
       const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > tile_r0) || (kj0 + C::BN > N) ||
                              (window > 0 && (kj0 < tile_r0 + C::BM - window ||
@@ -354,6 +358,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         uint32_t r[32];
         tmem_ld32(tbase + C::TM_DQ + c * 32, r);
         tmem_wait_ld();
+        tmem_reg_fence(r);
         if (valid) {
           uint32_t pk[16];
 #pragma unroll

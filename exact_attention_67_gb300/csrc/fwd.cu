@@ -432,6 +432,8 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
       tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_reg_fence(sr[c]);
       if constexpr (C::EARLY_S) {
         // S_t is in registers: the MMA warp may compute the next one over it.
         tc_fence_before();
@@ -517,6 +519,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
           uint32_t o_r[32];
           tmem_ld32(tO + c * 32, o_r);
           tmem_wait_ld();
+          tmem_reg_fence(o_r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o_r[e] = __float_as_uint(__uint_as_float(o_r[e]) * alpha);
           tmem_st32(tO + c * 32, o_r);
@@ -554,6 +557,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
         if (any) {
           tmem_ld32(tO + c * 32, o_r);
           tmem_wait_ld();
+          tmem_reg_fence(o_r);
         }
         if (row_g < N) {
           float4* dst = reinterpret_cast<float4*>(po + c * 32);
@@ -578,6 +582,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
         uint32_t o_r[32];
         tmem_ld32(tO + c * 32, o_r);
         tmem_wait_ld();
+        tmem_reg_fence(o_r);
         if (row_g < N) {
           uint32_t pk[16];
 #pragma unroll

@@ -84,10 +84,11 @@ __host__ __device__ __forceinline__ GridPos grid_pos(int block, int BH, int n_ti
 }
 
 // Problems per group for grid_pos: as many as keep their re-read operands
-// (bytes_per_problem each) within half of the 129 MB L2, at least one.
+// (bytes_per_problem each) within `budget` bytes of the 129 MB L2 (half of
+// it by default), at least one.
 constexpr long long kL2GroupBytes = 64ll << 20;
-inline int l2_group(long long bytes_per_problem, int BH) {
-  long long g = bytes_per_problem > 0 ? kL2GroupBytes / bytes_per_problem : BH;
+inline int l2_group(long long bytes_per_problem, int BH, long long budget = kL2GroupBytes) {
+  long long g = bytes_per_problem > 0 ? budget / bytes_per_problem : BH;
   if (g > BH) g = BH;
   return g < 1 ? 1 : static_cast<int>(g);
 }

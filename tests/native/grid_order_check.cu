@@ -34,7 +34,7 @@ int main() {
         }
   // Group sizes: 64 MB of re-read operand per group, at least one problem, at most B*H.
   if (l2_group(4ll << 20, 16) != 16 || l2_group(1ll << 20, 128) != 64 || l2_group(64ll << 20, 1) != 1 ||
-      l2_group(1ll << 30, 8) != 1 || l2_group(0, 5) != 5)
+      l2_group(1ll << 30, 8) != 1 || l2_group(0, 5) != 5 || l2_group(1ll << 20, 128, 32ll << 20) != 32)
     ++bad;
   std::printf("%lld cases, %lld mismatches\n", cases, bad);
   return bad != 0;
