@@ -31,8 +31,9 @@
 //     tile to f16 in shared memory, in place, between its TMA landing and its
 //     first P V (exact for 2^-14 <= |v| <= 65504 and for 0; smaller
 //     magnitudes are carried with an absolute error below 2^-25).
-//   * epilogue: O_t / l rounded to the input type, lse = (m + log2 l) ln 2;
-//     l for O sums the rounded P that the PV MMA used.
+//   * epilogue: O_t / l rounded to the input type, lse = (m + log2 l) ln 2,
+//     with l the sum of the f16-rounded P that the PV MMA used (one row sum:
+//     lse moves by at most 2^-12 against the sum of unrounded terms).
 // TMEM: FwdCfg (S, P, O of each tile).
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -158,8 +159,8 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->q_full[t], 1);
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->s_free[t], 128);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->s_free[t], 4);  // one arrival per softmax warp
+      mbar_init(&bars->p_full[t], 4);
       mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_full[t], 1);
     }
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
-      mbar_init(&bars->v_conv[s], 64);
+      mbar_init(&bars->v_conv[s], 2);  // one arrival per converting warp
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       const int ct = (warp - 10) * 32 + lane;
       for (int j = 0; j < n_iter; ++j) {
         const int s = j % C::STAGES;
-        if (!mbar_wait(&bars->v_full[s], (j / C::STAGES) & 1, wc)) break;
+        if (!mbar_wait_warp(&bars->v_full[s], (j / C::STAGES) & 1, wc)) break;
         uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_V + s * C::TILE_BYTES);
 #pragma unroll 1
         for (int b0 = 0; b0 < PER; b0 += BATCH) {
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
                                                   bf16x2_to_f16x2(x[u].z), bf16x2_to_f16x2(x[u].w));
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars->v_conv[s]);
+        mbar_arrive_warp(&bars->v_conv[s]);
       }
     }
   } else {
@@ -421,11 +422,10 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     const uint32_t tP = tmem + lane_bits + C::tm_p(t);
     const uint32_t tO = tmem + lane_bits + C::tm_o(t);
     float m_ref = -INFINITY;  // reference max, log2 units of the scaled logits
-    float l = 0.f;            // running sum of 2^(x - m_ref), fp32 terms (for lse)
-    float lb = 0.f;           // the same sum over the f16-rounded terms the PV MMA uses (for O)
+    float lb = 0.f;           // running sum of the f16-rounded 2^(x - m_ref) the PV MMA uses
     bool ok = true;  // cleared only by a wait that gave up
     for (int j = 0; ok && j < (t == 0 ? nkv0 : nkv1); ++j) {
-      if (!(ok = mbar_wait(&bars->s_full[t], j & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(&bars->s_full[t], j & 1, wc))) break;
       if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 0);
       tc_fence_after();
       uint32_t sr[4][32];
@@ -437,10 +437,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       if constexpr (C::EARLY_S) {
         // S_t is in registers: the MMA warp may compute the next one over it.
         tc_fence_before();
-        mbar_arrive(&bars->s_free[t]);
-        // P_t(j-1) V_{j-1} must be done before P_t and O_t are touched again.
-        if (j > 0 && !(ok = mbar_wait(&bars->pv_done[t], (j - 1) & 1, wc))) break;
-        tc_fence_after();
+        mbar_arrive_warp(&bars->s_free[t]);
       }
 
       const int kv0 = (kv_lo + j) * C::BN;
@@ -494,8 +491,6 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       // A row that has seen only masked keys so far (a window start inside a
       // later tile) keeps m_ref = -inf: its P is 0, never NaN.
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      // Packed partial sums: short FADD chains, half the instructions.
-      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
       uint32_t pk[4][16];  // P as f16 pairs, kept for the rounded sum below
 #pragma unroll
@@ -504,13 +499,19 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
         for (int e = 0; e < 16; ++e) {
           const float2 y = ffma2(make_float2(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])), sc2, nm2);
           const float2 p = make_float2(ex2(y.x), ex2(y.y));
-          rs[e & 1] = fadd2(rs[e & 1], p);
           pk[c][e] = PE::pack(p.x, p.y);
         }
-        tmem_st16(tP + c * 16, pk[c]);  // P_t (d = 128: over the first 64 columns of S_t)
+        if constexpr (!C::EARLY_S) tmem_st16(tP + c * 16, pk[c]);  // P_t over the first 64 columns of S_t
       }
-      const float2 r = fadd2(rs[0], rs[1]);
-      l = l * alpha + (r.x + r.y);
+      if constexpr (C::EARLY_S) {
+        // Only now must P_t(j-1) V_{j-1} be done (its P_t columns and the O_t
+        // row are written next): the maxima and exponentials above ran while
+        // the tensor core worked on it.
+        if (j > 0 && !(ok = mbar_wait_warp(&bars->pv_done[t], (j - 1) & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, pk[c]);  // P_t in its own columns
+      }
       if (rescale_warp) {
         // P_t(j-1) V_{j-1} has completed (d = 128: S_t(j) is issued after it;
         // d = 64: pv_done waited above): the O row is stable.
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       tmem_wait_st();
       tc_fence_before();
       if (row == 0) EXATTN_TRACE_POINT(2 + t, j, 1);
-      mbar_arrive(&bars->p_full[t]);
+      mbar_arrive_warp(&bars->p_full[t]);
       // O is normalised by the sum of the f16-rounded weights the PV MMA
       // used: a row dominated by a few keys then keeps an exact convex
       // combination of V rows instead of inheriting their rounding.  Done
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
         }
       }
       if (row_g < N) {
-        kv.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        kv.part_lse[prow] = lb > 0.f ? (m_ref + log2f(lb)) * 0.6931471805599453f : -INFINITY;
         kv.part_lseb[prow] = lb > 0.f ? (m_ref + log2f(lb)) * 0.6931471805599453f : -INFINITY;
       }
     } else if (ok && any) {
@@ -594,7 +595,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (row_g < N) lse_out[sr0.stat0 + row_g] = (m_ref + log2f(l)) * 0.6931471805599453f;
+      if (row_g < N) lse_out[sr0.stat0 + row_g] = (m_ref + log2f(lb)) * 0.6931471805599453f;
     }
   }
 
