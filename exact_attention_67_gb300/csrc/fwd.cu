@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-template <typename T, int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL, bool ONE_TILE>
 __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
   const int split = gp.sub;
   const int bh = gp.bh;
   const int hh = bh % H, bb = bh / H;  // head and batch index
-  const int q0 = pair * 2 * C::BM;
+  // A CTA owns two query tiles, or one (ONE_TILE: n_pairs then counts single
+  // tiles and tile 1 stays empty) when two-tile CTAs would leave SMs idle.
+  const int q0 = pair * (ONE_TILE ? 1 : 2) * C::BM;
   // This batch's rows (a packed variable-length batch may be shorter than the
   // grid's longest sequence: such a CTA has nothing to do).
   const SeqRows sr0 = seq_rows(seq, bb, hh, H, N_max);
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     const int e = key_end(t);
     return e == 0 ? 0 : max(0, min((e + C::BN - 1) / C::BN, split_hi) - kv_lo);
   };
-  const int nkv0 = tiles_for(0), nkv1 = tiles_for(1);
+  const int nkv0 = tiles_for(0), nkv1 = ONE_TILE ? 0 : tiles_for(1);
   const int n_iter = max(nkv0, nkv1);
 
   if (threadIdx.x == 0) {
@@ -516,8 +518,10 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
       }
       if (rescale_warp) {
         // P_t(j-1) V_{j-1} has completed (d = 128: S_t(j) is issued after it;
-        // d = 64: pv_done waited above): the O row is stable.
-#pragma unroll
+        // d = 64: pv_done waited above): the O row is stable.  This branch is
+        // rare; at d = 128 it runs rolled, which keeps the kernel inside its
+        // 168 registers without spills.
+#pragma unroll(D == 128 ? 1 : D / 32)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o_r[32];
           tmem_ld32(tO + c * 32, o_r);
@@ -610,15 +614,24 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
 template <typename T, int D, bool CAUSAL>
 static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<T, D, CAUSAL>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   KvSplit kv = a.kv;
   if (kv.n_splits < 1) {  // one CTA covers all keys of its query pair
     kv.n_splits = 1;
     kv.tiles_per_split = 1 << 30;
   }
-  const int n_pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  // Two query tiles per CTA share each K/V tile and hide each other's
+  // hand-offs; when that leaves at most one CTA per SM (small problems), one
+  // tile per CTA doubles the CTAs and halves the longest CTA's chain.
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, a.device);
+  if (e != cudaSuccess) return e;
+  const int pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  const bool one_tile = kv.n_splits == 1 && static_cast<long long>(pairs) * a.BH <= sms;
+  const int n_pairs = one_tile ? (a.N + C::BM - 1) / C::BM : pairs;
+  auto kern = one_tile ? attn_fwd_kernel<T, D, CAUSAL, true> : attn_fwd_kernel<T, D, CAUSAL, false>;
+  e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, a.device);
+  if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(n_pairs) * kv.n_splits * a.BH;
   // Group heads so their K and V stay in L2 -- except when the key splits read
   // disjoint key ranges (nothing is re-read across CTAs) or the packed
@@ -645,9 +658,10 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
 
 // ---------------------------------------------------------------- split merge
 // O and lse of query row r from the key splits' partials: with the splits'
-// logsumexps L_s (exact sums) and Lb_s (rounded weights), lse = log sum_s
-// exp(L_s) and O = sum_s exp(Lb_s - log sum_s' exp(Lb_s')) O_s -- the same
-// two normalisations the single-CTA forward uses, over all keys.  One
+// logsumexps L_s and Lb_s, lse = log sum_s exp(L_s) and O = sum_s exp(Lb_s -
+// log sum_s' exp(Lb_s')) O_s.  The forward writes both from its sum of the
+// f16-rounded weights (the one normalisation the single-CTA forward uses), so
+// L_s = Lb_s; the two inputs are kept in the workspace layout.  One
 // 256-thread block per row: the threads share the splits for the two
 // logsumexps, then 256 / d groups of d threads (one column each) share them
 // for O, and the groups' sums are added in shared memory.
