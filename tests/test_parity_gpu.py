@@ -124,6 +124,25 @@ def test_backward_is_deterministic():
     assert ex.device_error() == 0
 
 
+@pytest.mark.parametrize("d,causal,sigma", [(128, True, 1.0), (64, False, 1.0), (128, False, 4.0)])
+def test_one_and_two_query_tiles_per_cta_agree(d, causal, sigma):
+    """A grid of at most one wave runs one query tile per forward CTA, a larger
+    one two: the same head gives bit-identical O and lse either way.  Alone it
+    is 4 pairs of tiles (one tile per CTA); as head 0 of 200 heads, 800 pairs
+    (two tiles per CTA).  N = 1000 leaves a ragged last tile; sigma 4 makes
+    the running max move past 2^8 (the O rescale)."""
+    import exact_attention_67_gb300 as ex
+    w, (q, k, v, _) = custom(1, 200, 1000, d, causal, seed=4242, sigma_qk=sigma)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o_all, lse_all = ex.forward(q, k, v, causal, w.scale)
+    o_one, lse_one = ex.forward(q[:, :1].contiguous(), k[:, :1].contiguous(), v[:, :1].contiguous(), causal,
+                                w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_all[:, :1], o_one)
+    assert torch.equal(lse_all[:, :1], lse_one)
+    assert ex.device_error() == 0
+
+
 def test_arch_and_stream_semantics():
     """Launches are asynchronous on the given stream and honour stream order."""
     import exact_attention_67_gb300 as ex
