@@ -9,8 +9,8 @@
 // 黑洞…", 第一章, causal=True skips the upper triangle).
 //
 // GB300 mapping (one CTA per SM; 320 threads, 384 with bf16 inputs):
-//   * the CTA owns two 128-row query tiles (256 rows) of one (batch, head);
-//     they share one stream of 128-row K/V tiles;
+//   * the CTA owns two 128-row query tiles (256 rows) of one (batch, head),
+//     one on grids small enough for one wave; they share one K/V stream;
 //   * warp 8 issues TMA loads: both Q tiles once, then K_j and V_j into
 //     STAGES-deep rings of 128-byte-swizzled shared-memory tiles;
 //   * warp 9 (one thread) issues tcgen05 MMAs: S_t = Q_t K_j^T into TMEM

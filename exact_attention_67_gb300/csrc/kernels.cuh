@@ -99,8 +99,8 @@ inline int l2_group(long long bytes_per_problem, int BH, long long budget = kL2G
 // n_splits CTAs of tiles_per_split 128-key tiles each.  With part_o set,
 // every split writes fp32 partial results that launch_fwd_merge combines:
 //   part_o    [n_splits, B*H, nq_pad, d]  O of the split (normalised within it)
-//   part_lse  [n_splits, B*H, nq_pad]     logsumexp of the split (exact sum)
-//   part_lseb [n_splits, B*H, nq_pad]     logsumexp of the rounded weights
+//   part_lse  [n_splits, B*H, nq_pad]     logsumexp of the split (for lse)
+//   part_lseb [n_splits, B*H, nq_pad]     logsumexp of the rounded weights (for O)
 struct KvSplit {
   int nk;  // 0: as many keys as queries, no offset
   int n_splits, tiles_per_split, nq_pad;
