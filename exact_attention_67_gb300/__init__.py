@@ -18,13 +18,13 @@ from __future__ import annotations
 import math
 
 from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
-                   attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_decode, attn_fwd_bwd_host,
+                   attn_bwd_o32, attn_fwd_o32, attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_decode, attn_fwd_bwd_host,
                    attn_fwd_bwd_host_workspace_size, attn_fwd_decode_workspace_size, attn_fwd_ex, attn_fwd_varlen,
                    device_error, library_path, load, status_string, version, watchdog_check, watchdog_poll)
 from .host import HostStep, fwd_bwd_from_host
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex",
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_o32", "attn_bwd_o32",
            "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward", "backward", "forward_varlen", "backward_varlen", "attn_fwd_decode", "attn_fwd_decode_workspace_size",
            "forward_decode", "fwd_bwd_from_host", "HostStep", "attn_fwd_bwd_host",
            "attn_fwd_bwd_host_workspace_size", "attention", "flash_attn_func", "device_error",
@@ -41,17 +41,24 @@ def _plain(*ts) -> bool:
     return all(t.dtype == torch.bfloat16 and t.is_contiguous() for t in ts)
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None, window: int = 0):
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None, window: int = 0,
+            fp32_o: bool = False):
     """Allocate O (same type and memory layout as q) and lse (fp32) with torch
     and run ``attn_fwd`` (contiguous bf16) or ``attn_fwd_ex`` (f16 or strided
     [B, H, N, d] views, e.g. ``x.transpose(1, 2)`` of a [B, N, H, d] tensor, or
-    a sliding ``window`` > 0)."""
+    a sliding ``window`` > 0).  With ``fp32_o`` it runs ``attn_fwd_o32`` and
+    returns (O, lse, O in fp32) for ``backward(..., o32=...)``."""
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
     watchdog_check(q.device)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if fp32_o:
+        o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+        attn_fwd_o32(q, k, v, o, lse, o32, causal, s, stream, window)
+        watchdog_poll(q.device, stream)
+        return o, lse, o32
     if window == 0 and _plain(q, k, v, o):
         attn_fwd(q, k, v, o, lse, causal, s, stream)
     else:
@@ -61,9 +68,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, stream=None,
-             workspace=None, window: int = 0):
+             workspace=None, window: int = 0, o32=None):
     """Allocate dQ, dK, dV (like q, k, v) and the workspace unless given, and run
-    ``attn_bwd`` (contiguous bf16) or ``attn_bwd_ex``."""
+    ``attn_bwd`` (contiguous bf16) or ``attn_bwd_ex``; with ``o32`` (from
+    ``forward(..., fp32_o=True)``) ``attn_bwd_o32``, which takes the row terms
+    D_i from it and does not read ``o``."""
     import torch
     B, H, N, d = q.shape
     s = _default_scale(d) if scale is None else scale
@@ -72,7 +81,9 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     if workspace is None:
         nbytes = attn_bwd_workspace_size(B, H, N, d, causal)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    if window == 0 and _plain(q, k, v, o, dO, dq, dk, dv):
+    if o32 is not None:
+        attn_bwd_o32(q, k, v, o32, dO, lse, dq, dk, dv, causal, s, workspace, stream, window)
+    elif window == 0 and _plain(q, k, v, o, dO, dq, dk, dv):
         attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream)
     else:
         attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal, s, workspace, stream, window)

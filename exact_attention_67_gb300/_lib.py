@@ -16,6 +16,7 @@ _lock = threading.Lock()
 _lib = None
 
 EXATTN_OK = 0
+EXATTN_ERR_CUDA = 7
 STATUS_NAMES = {
     0: "EXATTN_OK", 1: "EXATTN_ERR_NULL", 2: "EXATTN_ERR_SHAPE", 3: "EXATTN_ERR_ALIGN",
     4: "EXATTN_ERR_UNSUPPORTED", 5: "EXATTN_ERR_ARCH", 6: "EXATTN_ERR_WORKSPACE",
@@ -23,10 +24,11 @@ STATUS_NAMES = {
 }
 # Every entry point include/exattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_varlen", "attn_bwd_varlen",
+           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_o32", "attn_bwd_o32", "attn_fwd_varlen",
+           "attn_bwd_varlen",
            "attn_fwd_decode_workspace_size", "attn_fwd_decode", "attn_bwd_noalloc",
            "attn_fwd_bwd_host_workspace_size", "attn_fwd_bwd_host",
-           "exattn_status_string",
+           "exattn_status_string", "exattn_last_cuda_error",
            "exattn_device_error", "exattn_device_error_poll", "exattn_watchdog_selftest", "exattn_version")
 
 EXATTN_DTYPE_BF16 = 0
@@ -82,6 +84,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_ex.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, i, i, i, i, i, i,
                                     f, vp, sz, vp]
         lib.attn_bwd_ex.restype = i
+        lib.attn_fwd_o32.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, vp, i, i, i, i, i, i, f, vp]
+        lib.attn_fwd_o32.restype = i
+        lib.attn_bwd_o32.argtypes = [i, vp, S, vp, S, vp, S, vp, vp, S, vp, vp, S, vp, S, vp, S, i, i, i, i, i, i, f,
+                                     vp, sz, vp]
+        lib.attn_bwd_o32.restype = i
         lib.attn_fwd_varlen.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.attn_fwd_varlen.restype = i
         lib.attn_bwd_varlen.argtypes = [i, vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, S, vp, S, vp, S, vp, i, i, i, i,
@@ -102,6 +109,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_workspace_size.restype = sz
         lib.exattn_status_string.argtypes = [i]
         lib.exattn_status_string.restype = ctypes.c_char_p
+        lib.exattn_last_cuda_error.argtypes = []
+        lib.exattn_last_cuda_error.restype = ctypes.c_char_p
         lib.exattn_device_error.argtypes = []
         lib.exattn_device_error.restype = i
         lib.exattn_watchdog_selftest.argtypes = [ctypes.c_uint, vp]
@@ -116,9 +125,18 @@ def status_string(status: int) -> str:
     return load().exattn_status_string(int(status)).decode()
 
 
+def last_cuda_error() -> str:
+    """C ``exattn_last_cuda_error``: the failing CUDA call behind the calling
+    thread's last EXATTN_ERR_CUDA ("" if none)."""
+    return load().exattn_last_cuda_error().decode()
+
+
 def _check(status: int):
     if status != EXATTN_OK:
-        raise ExattnError(status, status_string(status))
+        msg = status_string(status)
+        if status == EXATTN_ERR_CUDA:
+            msg += f" ({last_cuda_error()})"
+        raise ExattnError(status, msg)
 
 
 def _ptr(t):
@@ -223,6 +241,52 @@ def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, causal: bool, scale: float, wor
                                   _ptr(lse), _ptr(dq), s[4], _ptr(dk), s[5], _ptr(dv), s[6], B, H, N, d,
                                   int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
                                   _stream(stream, dev)))
+
+
+def _check_o32(o32, B, H, N, d):
+    if o32.dtype != torch.float32 or tuple(o32.shape) != (B, H, N, d) or not o32.is_contiguous():
+        raise ValueError("o32 must be contiguous float32 [B, H, N, d]")
+
+
+def attn_fwd_o32(q, k, v, o, lse, o32, causal: bool, scale: float, stream=None, window: int = 0) -> None:
+    """C ``attn_fwd_o32``: ``attn_fwd_ex`` that also writes ``o32``, an fp32
+    contiguous [B, H, N, d] copy of O before its rounding (for ``attn_bwd_o32``)."""
+    (B, H, N, d), dt, sq = _view4(q, "q")
+    views = [_view4(t, n) for n, t in (("k", k), ("v", v), ("o", o))]
+    for n, (shape, dtn, _) in zip(("k", "v", "o"), views):
+        if shape != (B, H, N, d) or dtn != dt:
+            raise ValueError(f"{n} shape/dtype differs from q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    _check_o32(o32, B, H, N, d)
+    dev = _device_of(q, k, v, o, lse, o32)
+    with torch.cuda.device(dev):
+        _check(load().attn_fwd_o32(dt, _ptr(q), sq, _ptr(k), views[0][2], _ptr(v), views[1][2], _ptr(o),
+                                   views[2][2], _ptr(lse), _ptr(o32), B, H, N, d, int(bool(causal)), int(window),
+                                   float(scale), _stream(stream, dev)))
+
+
+def attn_bwd_o32(q, k, v, o32, dO, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None,
+                 window: int = 0) -> None:
+    """C ``attn_bwd_o32``: ``attn_bwd_ex`` with the row terms D_i taken from the
+    fp32 ``o32`` that ``attn_fwd_o32`` wrote (O itself is not needed)."""
+    (B, H, N, d), dt, sq = _view4(q, "q")
+    names = ("k", "v", "dO", "dq", "dk", "dv")
+    views = [_view4(t, n) for n, t in zip(names, (k, v, dO, dq, dk, dv))]
+    for n, (shape, dtn, _) in zip(names, views):
+        if shape != (B, H, N, d) or dtn != dt:
+            raise ValueError(f"{n} shape/dtype differs from q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    _check_o32(o32, B, H, N, d)
+    s = [vw[2] for vw in views]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dev = _device_of(q, k, v, o32, dO, lse, dq, dk, dv, workspace)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_o32(dt, _ptr(q), sq, _ptr(k), s[0], _ptr(v), s[1], _ptr(o32), _ptr(dO), s[2],
+                                   _ptr(lse), _ptr(dq), s[3], _ptr(dk), s[4], _ptr(dv), s[5], B, H, N, d,
+                                   int(bool(causal)), int(window), float(scale), _ptr(workspace), ws_bytes,
+                                   _stream(stream, dev)))
 
 
 def _packed3(t: torch.Tensor, name: str):

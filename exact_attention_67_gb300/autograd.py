@@ -16,16 +16,20 @@ from . import forward as _forward
 
 class _Attention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal: bool, scale, window: int):
-        o, lse = _forward(q, k, v, causal, scale, window=window)
-        ctx.save_for_backward(q, k, v, o, lse)
-        ctx.causal, ctx.scale, ctx.window = causal, scale, window
+    def forward(ctx, q, k, v, causal: bool, scale, window: int, fp32_o: bool):
+        if fp32_o:
+            o, lse, o32 = _forward(q, k, v, causal, scale, window=window, fp32_o=True)
+            ctx.save_for_backward(q, k, v, o32, lse)
+        else:
+            o, lse = _forward(q, k, v, causal, scale, window=window)
+            ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale, ctx.window, ctx.fp32_o = causal, scale, window, fp32_o
         return o
 
     @staticmethod
     @torch.autograd.function.once_differentiable
     def backward(ctx, do):
-        q, k, v, o, lse = ctx.saved_tensors
+        q, k, v, o_saved, lse = ctx.saved_tensors
         # The library reads dO through its strides (d contiguous, other strides
         # multiples of 8 elements, nonzero) from a 16-byte-aligned address: an
         # expanded, oddly strided or offset gradient (e.g. from
@@ -34,15 +38,20 @@ class _Attention(torch.autograd.Function):
         if (do.stride(-1) != 1 or any(s == 0 or s % 8 for s in do.stride()[:-1]) or
                 do.data_ptr() % 16 != 0):
             do = do.contiguous()
-        dq, dk, dv = _backward(q, k, v, o, lse, do, ctx.causal, ctx.scale, window=ctx.window)
-        return dq, dk, dv, None, None, None
+        if ctx.fp32_o:
+            dq, dk, dv = _backward(q, k, v, None, lse, do, ctx.causal, ctx.scale, window=ctx.window, o32=o_saved)
+        else:
+            dq, dk, dv = _backward(q, k, v, o_saved, lse, do, ctx.causal, ctx.scale, window=ctx.window)
+        return dq, dk, dv, None, None, None, None
 
 
-def attention(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0):
+def attention(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0, fp32_o: bool = False):
     """O = softmax(scale Q K^T [+ causal mask, sliding window]) V for [B, H, N, d]
     bf16/f16 CUDA tensors (any layout with d contiguous), differentiable in q,
-    k and v.  scale defaults to 1/sqrt(d)."""
-    return _Attention.apply(q, k, v, bool(causal), scale, int(window))
+    k and v.  scale defaults to 1/sqrt(d).  ``fp32_o`` keeps an fp32 copy of O
+    for the backward's row terms (B*H*N*d*4 bytes until backward): accurate
+    gradients also on rows whose softmax is nearly one-hot."""
+    return _Attention.apply(q, k, v, bool(causal), scale, int(window), bool(fp32_o))
 
 
 def flash_attn_func(q, k, v, dropout_p: float = 0.0, softmax_scale: float | None = None, causal: bool = False):

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -39,6 +40,7 @@ namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
 constexpr int kMaxDevices = 64;
 
@@ -51,6 +53,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
+CtxGetCurrentFn g_ctx_current = nullptr;
 
 struct AttrKey {
   const void* fn;
@@ -61,42 +64,76 @@ int g_attr_count = 0;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Arch check, watchdog address and the tensor-map encoder, once per device.
+// The last CUDA call that failed on this host thread (exattn_last_cuda_error).
+thread_local const char* t_fail_call = nullptr;
+thread_local int t_fail_code = 0;
+thread_local bool t_fail_driver = false;
+thread_local char t_fail_text[192];
+
+// A driver entry point by name (CUDA 12.0 ABI); false if it is missing.
+bool driver_fn(const char* name, void** fn) {
+  cudaDriverEntryPointQueryResult q;
+  if (note_cuda(cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q),
+                "cudaGetDriverEntryPointByVersion") != cudaSuccess)
+    return false;
+  if (q != cudaDriverEntryPointSuccess || !*fn) {
+    note_failure("cudaGetDriverEntryPointByVersion (driver entry point not found)", static_cast<int>(q), false);
+    return false;
+  }
+  return true;
+}
+
+// Arch check, watchdog address and the driver entry points, once per device;
+// then, on every call, the device's primary context made current if the
+// calling host thread has none.  A thread that has made no CUDA call yet has
+// no current context, and the tensor-map encoder, a driver call, fails in it
+// with CUDA_ERROR_INVALID_CONTEXT; cudaSetDevice makes the primary context
+// current (the one the kernels already run in).
 int device_setup(int* dev_out, unsigned** err_out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return EXATTN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return EXATTN_ERR_CUDA;
+  if (note_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) {
+    note_failure("cudaGetDevice (device ordinal out of range)", static_cast<int>(cudaErrorInvalidDevice), false);
+    return EXATTN_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    if (note_cuda(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute") !=
+            cudaSuccess ||
+        note_cuda(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute") !=
+            cudaSuccess) {
       return EXATTN_ERR_CUDA;
     }
     if (major != 10 || minor != 3) {
       st.status = EXATTN_ERR_ARCH;
     } else {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return EXATTN_ERR_CUDA;
+      if (note_cuda(cudaGetSymbolAddress(&p, g_err_word), "cudaGetSymbolAddress") != cudaSuccess)
+        return EXATTN_ERR_CUDA;
       st.err = static_cast<unsigned*>(p);
-      if (!g_encode) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn) {
-          return EXATTN_ERR_CUDA;
-        }
-        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      if (!g_encode || !g_ctx_current) {
+        void *enc = nullptr, *cur = nullptr;
+        if (!driver_fn("cuTensorMapEncodeTiled", &enc) || !driver_fn("cuCtxGetCurrent", &cur)) return EXATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(enc);
+        g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(cur);
       }
       st.status = EXATTN_OK;
     }
     st.ready = true;
   }
+  if (st.status != EXATTN_OK) return st.status;
+  CUcontext ctx = nullptr;
+  const CUresult r = g_ctx_current(&ctx);
+  if (r != CUDA_SUCCESS) {
+    note_failure("cuCtxGetCurrent", static_cast<int>(r), true);
+    return EXATTN_ERR_CUDA;
+  }
+  if (!ctx && note_cuda(cudaSetDevice(dev), "cudaSetDevice") != cudaSuccess) return EXATTN_ERR_CUDA;
   *dev_out = dev;
   *err_out = st.err;
-  return st.status;
+  return EXATTN_OK;
 }
 
 // A [B, H, N, d] view (d contiguous, element strides s) as a 4-D map
@@ -112,9 +149,11 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int N, 
   const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType ty = dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  return g_encode(m, ty, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = g_encode(m, ty, 4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) note_failure("cuTensorMapEncodeTiled", static_cast<int>(r), true);
+  return r == CUDA_SUCCESS;
 }
 
 int check_common(int B, int H, int N, int d, float scale) {
@@ -146,11 +185,18 @@ int check_strides(const exattn_strides& s, int B, int H, int N) {
 
 }  // namespace
 
+void note_failure(const char* call, int code, bool driver) {
+  t_fail_call = call;
+  t_fail_code = code;
+  t_fail_driver = driver;
+}
+
 cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device) {
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < g_attr_count; ++i)
     if (g_attr_done[i].fn == kernel && g_attr_done[i].device == device) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = note_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                            "cudaFuncSetAttribute");
   if (e != cudaSuccess) return e;
   if (g_attr_count < 256) g_attr_done[g_attr_count++] = AttrKey{kernel, device};
   return cudaSuccess;
@@ -166,7 +212,8 @@ namespace {
 // variable-length sequences, seq.cu_seqlens set) one batch of seq.total rows.
 int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const Strides& sk, const void* v,
              const Strides& sv, void* o, const Strides& so, float* lse, int B, int H, int N, int d, int causal,
-             int window, float scale, void* stream, const SeqView& seq = SeqView{nullptr, 0}) {
+             int window, float scale, void* stream, const SeqView& seq = SeqView{nullptr, 0},
+             float* o32 = nullptr) {
   int dev = 0;
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
@@ -191,6 +238,7 @@ int fwd_impl(int dtype, const void* q, const Strides& sq, const void* k, const S
   a.dtype = dtype;
   a.window = window;
   a.seq = seq;
+  a.o32 = o32;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.err = err;
   a.device = dev;
@@ -225,6 +273,25 @@ extern "C" int attn_fwd_ex(int dtype, const void* q, exattn_strides sq, const vo
     if ((rc = check_strides(*s, B, H, N)) != EXATTN_OK) return rc;
   return fwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, q, to_strides(sq), k, to_strides(sk), v, to_strides(sv),
                   o, to_strides(so), lse, B, H, N, d, causal, window, scale, stream);
+}
+
+extern "C" int attn_fwd_o32(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                            const void* v, exattn_strides sv, void* o, exattn_strides so, float* lse, float* o32,
+                            int B, int H, int N, int d, int causal, int window, float scale, void* stream) {
+  if (!o32) return EXATTN_ERR_NULL;
+  if (!aligned(o32, 16)) return EXATTN_ERR_ALIGN;
+  if (!q || !k || !v || !o || !lse) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (window < 0) return EXATTN_ERR_VALUE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  const exattn_strides* all[4] = {&sq, &sk, &sv, &so};
+  for (const exattn_strides* s : all)
+    if ((rc = check_strides(*s, B, H, N)) != EXATTN_OK) return rc;
+  return fwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, q, to_strides(sq), k, to_strides(sk), v, to_strides(sv),
+                  o, to_strides(so), lse, B, H, N, d, causal, window, scale, stream, SeqView{nullptr, 0}, o32);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d, int causal) {
@@ -293,7 +360,7 @@ BwdInputs contiguous_inputs(const void* q, const void* k, const void* v, const v
 int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, const Strides& sdo, const float* lse,
              void* dq, const Strides& sdq, void* dk, const Strides& sdk, void* dv, const Strides& sdv, int B, int H,
              int N, int d, int causal, int window, float scale, void* workspace, void* stream,
-             const SeqView& seq = SeqView{nullptr, 0}) {
+             const SeqView& seq = SeqView{nullptr, 0}, const float* o32 = nullptr) {
   BwdArgs a{};
   BwdMaps maps;
   int rc = bwd_setup(a, maps, dtype, in, B, H, N, d, causal, scale, window, seq);
@@ -310,6 +377,7 @@ int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, c
   a.dv = dv;
   a.sdv = sdv;
   a.D = static_cast<float*>(workspace);
+  a.o32 = o32;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_bwd_prep(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
   if (launch_bwd_dkdv(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
@@ -419,6 +487,31 @@ extern "C" int attn_bwd_ex(int dtype, const void* q, exattn_strides sq, const vo
   return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, o, to_strides(so), to_strides(sdo), lse, dq,
                   to_strides(sdq), dk, to_strides(sdk), dv, to_strides(sdv), B, H, N, d, causal, window, scale,
                   workspace, stream);
+}
+
+extern "C" int attn_bwd_o32(int dtype, const void* q, exattn_strides sq, const void* k, exattn_strides sk,
+                            const void* v, exattn_strides sv, const float* o32, const void* dO, exattn_strides sdo,
+                            const float* lse, void* dq, exattn_strides sdq, void* dk, exattn_strides sdk, void* dv,
+                            exattn_strides sdv, int B, int H, int N, int d, int causal, int window, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o32 || !dO || !lse || !dq || !dk || !dv) return EXATTN_ERR_NULL;
+  if (dtype != EXATTN_DTYPE_BF16 && dtype != EXATTN_DTYPE_F16) return EXATTN_ERR_UNSUPPORTED;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (window < 0) return EXATTN_ERR_VALUE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o32, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return EXATTN_ERR_ALIGN;
+  const exattn_strides* all[7] = {&sq, &sk, &sv, &sdo, &sdq, &sdk, &sdv};
+  for (const exattn_strides* s : all)
+    if ((rc = check_strides(*s, B, H, N)) != EXATTN_OK) return rc;
+  if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, N, d, causal)) return EXATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return EXATTN_ERR_ALIGN;
+  const BwdInputs in{{q, k, v, dO}, {to_strides(sq), to_strides(sk), to_strides(sv), to_strides(sdo)}};
+  const Strides c = contiguous(H, N, d);  // o32's layout (O itself is not read)
+  return bwd_impl(dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16, in, nullptr, c, to_strides(sdo), lse, dq, to_strides(sdq),
+                  dk, to_strides(sdk), dv, to_strides(sdv), B, H, N, d, causal, window, scale, workspace, stream,
+                  SeqView{nullptr, 0}, o32);
 }
 
 namespace {
@@ -599,12 +692,14 @@ extern "C" int exattn_device_error(void) {
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
   if (rc != EXATTN_OK) return rc;
-  if (cudaDeviceSynchronize() != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (note_cuda(cudaDeviceSynchronize(), "cudaDeviceSynchronize") != cudaSuccess) return EXATTN_ERR_CUDA;
   unsigned v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(v)) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (note_cuda(cudaMemcpyFromSymbol(&v, g_err_word, sizeof(v)), "cudaMemcpyFromSymbol") != cudaSuccess)
+    return EXATTN_ERR_CUDA;
   if (v != 0) {
     const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return EXATTN_ERR_CUDA;
+    if (note_cuda(cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)), "cudaMemcpyToSymbol") != cudaSuccess)
+      return EXATTN_ERR_CUDA;
     return EXATTN_ERR_TIMEOUT;
   }
   return EXATTN_OK;
@@ -616,8 +711,9 @@ extern "C" int exattn_device_error_poll(unsigned* host_dst, void* stream) {
   unsigned* err = nullptr;
   int rc = device_setup(&dev, &err);
   if (rc != EXATTN_OK) return rc;
-  return cudaMemcpyAsync(host_dst, err, sizeof(unsigned), cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
+  return note_cuda(cudaMemcpyAsync(host_dst, err, sizeof(unsigned), cudaMemcpyDeviceToHost,
+                                   static_cast<cudaStream_t>(stream)),
+                   "cudaMemcpyAsync") == cudaSuccess
              ? EXATTN_OK
              : EXATTN_ERR_CUDA;
 }
@@ -629,7 +725,17 @@ extern "C" int exattn_watchdog_selftest(unsigned timeout_us, void* stream) {
   int rc = device_setup(&dev, &err);
   if (rc != EXATTN_OK) return rc;
   watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1000ull * timeout_us, err);
-  return cudaGetLastError() == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+  return note_cuda(cudaGetLastError(), "watchdog self-test kernel launch") == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
-extern "C" int exattn_version(void) { return 201; }  // 0.2.1: exattn_device_error_poll
+extern "C" const char* exattn_last_cuda_error(void) {
+  if (!t_fail_call) return "";
+  if (t_fail_driver)
+    std::snprintf(t_fail_text, sizeof(t_fail_text), "%s: CUresult %d", t_fail_call, t_fail_code);
+  else
+    std::snprintf(t_fail_text, sizeof(t_fail_text), "%s: %s (%d)", t_fail_call,
+                  cudaGetErrorName(static_cast<cudaError_t>(t_fail_code)), t_fail_code);
+  return t_fail_text;
+}
+
+extern "C" int exattn_version(void) { return 202; }  // 0.2.2: fp32-O calls, exattn_last_cuda_error

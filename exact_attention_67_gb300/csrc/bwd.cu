@@ -33,6 +33,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o, Strides so,
                                                          const T* __restrict__ dO, Strides sdo,
+                                                         const float* __restrict__ o32,
                                                          float* __restrict__ Dout, long long rows, int N, int H,
                                                          bool contiguous) {
   constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
@@ -53,16 +54,29 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o
         orow = o + b * so.b + h * so.h + n * so.n;
         drow = dO + b * sdo.b + h * sdo.h + n * sdo.n;
       }
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(orow) + part);
       const uint4 c = __ldg(reinterpret_cast<const uint4*>(drow) + part);
-      const uint32_t* a2 = reinterpret_cast<const uint32_t*>(&a);
       const uint32_t* c2 = reinterpret_cast<const uint32_t*>(&c);
+      if (o32 != nullptr) {
+        // O in fp32 (contiguous rows): the same 8 elements as two float4.
+        const float4* o4 = reinterpret_cast<const float4*>(o32 + r * D) + 2 * part;
+        const float4 a0 = __ldg(o4), a1 = __ldg(o4 + 1);
+        const float fa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 fa = Elem<T>::unpack(a2[e]);
-        const float2 fc = Elem<T>::unpack(c2[e]);
-        acc = fmaf(fa.x, fc.x, acc);
-        acc = fmaf(fa.y, fc.y, acc);
+        for (int e = 0; e < 4; ++e) {
+          const float2 fc = Elem<T>::unpack(c2[e]);
+          acc = fmaf(fa[2 * e], fc.x, acc);
+          acc = fmaf(fa[2 * e + 1], fc.y, acc);
+        }
+      } else {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(orow) + part);
+        const uint32_t* a2 = reinterpret_cast<const uint32_t*>(&a);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = Elem<T>::unpack(a2[e]);
+          const float2 fc = Elem<T>::unpack(c2[e]);
+          acc = fmaf(fa.x, fc.x, acc);
+          acc = fmaf(fa.y, fc.y, acc);
+        }
       }
     }
 #pragma unroll
@@ -503,12 +517,14 @@ static cudaError_t launch_prep_t(const BwdArgs& a, cudaStream_t stream) {
   const int rpb = 256 / (D / 8);  // rows per 256-thread block
   long long blocks = (rows + rpb - 1) / rpb;
   if (blocks > 152 * 16) blocks = 152 * 16;
+  // "contiguous": O and dO both [B, H, N, d] packed (O unused when the fp32
+  // copy o32, always packed, replaces it).
+  const Strides& so = a.o32 ? a.sdo : a.so;
   bwd_rowdot_kernel<T, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.D, rows, n_rows, a.H,
-      a.so.n == D && a.so.h == static_cast<long long>(n_rows) * D &&
-          a.so.b == static_cast<long long>(a.H) * n_rows * D && a.sdo.n == a.so.n && a.sdo.h == a.so.h &&
-          a.sdo.b == a.so.b);
-  return cudaGetLastError();
+      static_cast<const T*>(a.o), a.so, static_cast<const T*>(a.dO), a.sdo, a.o32, a.D, rows, n_rows, a.H,
+      so.n == D && so.h == static_cast<long long>(n_rows) * D && so.b == static_cast<long long>(a.H) * n_rows * D &&
+          a.sdo.n == so.n && a.sdo.h == so.h && a.sdo.b == so.b);
+  return note_cuda(cudaGetLastError(), "row-dot kernel launch");
 }
 
 template <typename T, int D, bool CAUSAL>
@@ -526,7 +542,7 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
       static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
-  return cudaGetLastError();
+  return note_cuda(cudaGetLastError(), "dK/dV kernel launch");
 }
 
 template <typename T>

@@ -392,7 +392,7 @@ static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
       *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<T*>(a.dq), a.sdq, a.N, a.H,
       a.BH, n_pairs, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
-  return cudaGetLastError();
+  return note_cuda(cudaGetLastError(), "dQ kernel launch");
 }
 
 template <typename T>

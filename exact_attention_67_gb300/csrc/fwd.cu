@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, Strides so,
                     float* __restrict__ lse_out, int N_max, int H, int BH, int n_pairs, int group, int window,
-                    float scale_log2, SeqView seq, KvSplit kv, unsigned* err) {
+                    float scale_log2, SeqView seq, KvSplit kv, float* __restrict__ o32, unsigned* err) {
   using C = FwdCfg<D>;
   using E = Elem<T>;
   using PE = Elem<__half>;  // P and the converted V: the P V product runs in f16
@@ -599,6 +599,16 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          if (o32 != nullptr) {
+            // The same row before rounding to the output type, for a backward
+            // that takes D_i = dO_i . O_i from it.
+            float4* dst32 = reinterpret_cast<float4*>(o32 + (static_cast<long long>(bh) * N_max + row_g) * D + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst32[v4] = make_float4(__uint_as_float(o_r[4 * v4]) * inv_l, __uint_as_float(o_r[4 * v4 + 1]) * inv_l,
+                                      __uint_as_float(o_r[4 * v4 + 2]) * inv_l,
+                                      __uint_as_float(o_r[4 * v4 + 3]) * inv_l);
+          }
         }
       }
       if (row_g < N) lse_out[sr0.stat0 + row_g] = (m_ref + log2f(lb)) * 0.6931471805599453f;
@@ -626,7 +636,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   // 0.0133 -> 0.0109 ms); at 128 pairs it gained nothing, and in the host
   // pipeline, whose head groups share the SMs on two streams, it cost 6 %.
   int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, a.device);
+  e = note_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, a.device), "cudaDeviceGetAttribute");
   if (e != cudaSuccess) return e;
   const int pairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   const bool one_tile = kv.n_splits == 1 && 2ll * pairs * a.BH <= sms;
@@ -648,8 +658,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
                                    kL2GroupBytes / 2);
   kern<<<static_cast<unsigned>(grid), FwdThreads<T>::value, C::SMEM_BYTES, stream>>>(
       *a.tm_q, *a.tm_k, *a.tm_v, static_cast<T*>(a.o), a.so, a.lse, a.N, a.H, a.BH, n_pairs, group, a.window,
-      a.scale_log2, a.seq, kv, a.err);
-  return cudaGetLastError();
+      a.scale_log2, a.seq, kv, a.o32, a.err);
+  return note_cuda(cudaGetLastError(), "forward kernel launch");
 }
 
 template <typename T>
@@ -745,12 +755,12 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const float* 
 
 template <typename T, int D>
 static cudaError_t launch_merge_t(const FwdArgs& a, cudaStream_t stream) {
-  if (a.kv.n_splits > kMaxSplits) return cudaErrorInvalidValue;
+  if (a.kv.n_splits > kMaxSplits) return note_cuda(cudaErrorInvalidValue, "split merge (too many key splits)");
   const long long rows = static_cast<long long>(a.BH) * a.N;
   attn_merge_kernel<T, D><<<static_cast<unsigned>(rows), kMergeThreads, 0, stream>>>(
       a.kv.part_o, a.kv.part_lse, a.kv.part_lseb, a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH,
       static_cast<T*>(a.o), a.so, a.lse);
-  return cudaGetLastError();
+  return note_cuda(cudaGetLastError(), "split-merge kernel launch");
 }
 
 cudaError_t launch_fwd_merge(const FwdArgs& a, cudaStream_t stream) {

@@ -13,6 +13,9 @@
 #include <cuda_runtime.h>
 
 #include "exattn.h"
+#include "kernels.cuh"
+
+using exattn::note_cuda;
 
 namespace {
 
@@ -47,7 +50,8 @@ struct Events {
   std::vector<cudaEvent_t> ev;
   cudaEvent_t make() {
     cudaEvent_t e = nullptr;
-    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (note_cuda(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreateWithFlags") != cudaSuccess)
+      return nullptr;
     ev.push_back(e);
     return e;
   }
@@ -60,7 +64,8 @@ struct Events {
 bool order(Events& E, cudaStream_t a, cudaStream_t b) {
   if (a == b) return true;
   cudaEvent_t e = E.make();
-  return e && cudaEventRecord(e, a) == cudaSuccess && cudaStreamWaitEvent(b, e, 0) == cudaSuccess;
+  return e && note_cuda(cudaEventRecord(e, a), "cudaEventRecord") == cudaSuccess &&
+         note_cuda(cudaStreamWaitEvent(b, e, 0), "cudaStreamWaitEvent") == cudaSuccess;
 }
 
 }  // namespace
@@ -106,12 +111,12 @@ extern "C" int attn_fwd_bwd_host(int dtype, const void* q, const void* k, const 
     const int a = static_cast<int>(static_cast<long long>(g) * BH / G);
     const int b = static_cast<int>(static_cast<long long>(g + 1) * BH / G);
     for (int i = 0; i < 4; ++i) {
-      if (cudaMemcpyAsync(dev_t(i, a), host_in(i, a), (b - a) * row_bytes, cudaMemcpyHostToDevice, sin) !=
-          cudaSuccess)
+      if (note_cuda(cudaMemcpyAsync(dev_t(i, a), host_in(i, a), (b - a) * row_bytes, cudaMemcpyHostToDevice, sin),
+                    "cudaMemcpyAsync (host to device)") != cudaSuccess)
         return EXATTN_ERR_CUDA;
       if (i == 2 || i == 3) {
         cudaEvent_t e = E.make();
-        if (!e || cudaEventRecord(e, sin) != cudaSuccess) return EXATTN_ERR_CUDA;
+        if (!e || note_cuda(cudaEventRecord(e, sin), "cudaEventRecord") != cudaSuccess) return EXATTN_ERR_CUDA;
         (i == 2 ? ev_qkv : ev_do)[g] = e;
       }
     }
@@ -133,11 +138,13 @@ extern "C" int attn_fwd_bwd_host(int dtype, const void* q, const void* k, const 
                            : static_cast<void*>(static_cast<uint8_t*>(hout[i]) + static_cast<size_t>(a) * row_bytes);
         const void* src = is_lse ? static_cast<const void*>(dev_lse(a)) : static_cast<const void*>(dev_t(4 + i, a));
         const size_t bytes = is_lse ? static_cast<size_t>(n) * N * 4 : n * row_bytes;
-        if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, sout) != cudaSuccess) return false;
+        if (note_cuda(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, sout),
+                      "cudaMemcpyAsync (device to host)") != cudaSuccess)
+          return false;
       }
       return true;
     };
-    if (cudaStreamWaitEvent(c, ev_qkv[g], 0) != cudaSuccess) return EXATTN_ERR_CUDA;
+    if (note_cuda(cudaStreamWaitEvent(c, ev_qkv[g], 0), "cudaStreamWaitEvent") != cudaSuccess) return EXATTN_ERR_CUDA;
     const exattn_strides cs{static_cast<long long>(n) * N * d, static_cast<long long>(N) * d, d};
     int rc = bf16 ? attn_fwd(dev_t(0, a), dev_t(1, a), dev_t(2, a), dev_t(4, a), dev_lse(a), 1, n, N, d, causal, scale,
                              c)
@@ -145,7 +152,7 @@ extern "C" int attn_fwd_bwd_host(int dtype, const void* q, const void* k, const 
                                 1, n, N, d, causal, 0, scale, c);
     if (rc != EXATTN_OK) return rc;
     if (!copy_out({0, -1})) return EXATTN_ERR_CUDA;  // O and lse leave while the backward runs
-    if (cudaStreamWaitEvent(c, ev_do[g], 0) != cudaSuccess) return EXATTN_ERR_CUDA;
+    if (note_cuda(cudaStreamWaitEvent(c, ev_do[g], 0), "cudaStreamWaitEvent") != cudaSuccess) return EXATTN_ERR_CUDA;
     if (bf16) {
       if ((rc = attn_bwd_preprocess(dev_t(4, a), dev_t(3, a), D, 1, n, N, d, c)) != EXATTN_OK) return rc;
       if ((rc = attn_bwd_dkdv(dev_t(0, a), dev_t(1, a), dev_t(2, a), dev_t(3, a), dev_lse(a), D, dev_t(6, a),

@@ -120,6 +120,7 @@ struct FwdArgs {
   int window;               // 0, or W >= 1: key j visible to query i iff i - j < W (and j - i < W if not causal)
   SeqView seq;              // N is the longest sequence when seq.cu_seqlens is set
   KvSplit kv;               // decode-shaped problems (kv.nk > 0); zero otherwise
+  float* o32;               // optional fp32 copy of O, contiguous [B*H, N, d] (fixed-length calls), or nullptr
   float scale_log2;         // scale * log2(e)
   unsigned* err;            // device watchdog word
   int device;
@@ -148,6 +149,7 @@ struct BwdArgs {
   Strides sdv;
   const float* lse;         // fp32 [B*H, N], natural log
   float* D;                 // workspace: fp32 [B*H, N]
+  const float* o32;         // optional fp32 O, contiguous [B*H, N, d]: D_i from it instead of o
   int N, H, BH, d, causal, dtype;
   int window;               // as FwdArgs::window
   SeqView seq;              // as FwdArgs::seq
@@ -155,6 +157,16 @@ struct BwdArgs {
   unsigned* err;
   int device;
 };
+
+// Records, for the calling host thread, a CUDA call that failed (`driver`:
+// `code` is a CUresult, else a cudaError_t); exattn_last_cuda_error() reads
+// it back.  note_cuda passes a runtime status through, recording it if it
+// is an error.
+void note_failure(const char* call, int code, bool driver);
+inline cudaError_t note_cuda(cudaError_t e, const char* call) {
+  if (e != cudaSuccess) note_failure(call, static_cast<int>(e), false);
+  return e;
+}
 
 cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);

@@ -36,11 +36,17 @@ float* g_noalloc_ptr[kMaxDev] = {};
 // Device address of this device's scratch array (set-up on first use).
 int noalloc_scratch(float** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return EXATTN_ERR_CUDA;
+  if (note_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDev) {
+    note_failure("cudaGetDevice (device ordinal out of range)", static_cast<int>(cudaErrorInvalidDevice), false);
+    return EXATTN_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     float* p = nullptr;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch) != cudaSuccess || !p)
+    if (note_cuda(cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch), "cudaGetSymbolAddress") !=
+            cudaSuccess ||
+        !p)
       return EXATTN_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
   }

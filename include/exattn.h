@@ -182,6 +182,32 @@ int attn_bwd_ex(int dtype, const void* q, exattn_strides q_strides, const void* 
                 int causal, int window, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The backward's row terms D_i = dO_i . O_i ("Gemini 3 Flash的注意力内核重写：
+ * 算子融合如何实现亚毫秒级推理", §4 重计算: recompute from the stored row
+ * statistics) taken from an fp32 copy of O instead of the O rounded to the
+ * input type.  Where a row's softmax puts nearly all its weight on one key,
+ * dS = P (dP - D) is a small difference and the 16-bit rounding of O
+ * dominates it: on such rows the fp32 copy keeps the gradients within the
+ * relative bound (a two-token sequence with weights 0.96 / 0.04: dQ relative
+ * error 0.10 from the bf16 O, 1.5e-4 from the fp32 copy).  It costs a
+ * d x 4-byte row per query in device memory and writes.
+ *   attn_fwd_o32 -- attn_fwd_ex that also writes o32: fp32, contiguous
+ *     [B, H, N, d], 16-byte aligned, owned by the caller; each row is the
+ *     normalised O before its rounding to the output type.  Errors as
+ *     attn_fwd_ex; a NULL o32 returns EXATTN_ERR_NULL.
+ *   attn_bwd_o32 -- attn_bwd_ex with o32 (as attn_fwd_o32 wrote it) in place
+ *     of O, which is not read.  Results and errors as attn_bwd_ex.
+ */
+int attn_fwd_o32(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                 const void* v, exattn_strides v_strides, void* o, exattn_strides o_strides, float* lse, float* o32,
+                 int B, int H, int N, int d, int causal, int window, float scale, void* stream);
+int attn_bwd_o32(int dtype, const void* q, exattn_strides q_strides, const void* k, exattn_strides k_strides,
+                 const void* v, exattn_strides v_strides, const float* o32, const void* dO, exattn_strides do_strides,
+                 const float* lse, void* dq, exattn_strides dq_strides, void* dk, exattn_strides dk_strides, void* dv,
+                 exattn_strides dv_strides, int B, int H, int N, int d, int causal, int window, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Packed variable-length batches.  The masked_flash_attention sketch of
  * "Flash Attention V3：大模型加速的核心网络算子优化实践", §三.3, pads
  * variable-length sequences and masks the padding with a [batch, 1, seq,
@@ -307,6 +333,16 @@ int attn_fwd_bwd_host(int dtype, const void* q, const void* k, const void* v, co
 
 /* Human-readable text of an exattn_status (static storage, never NULL). */
 const char* exattn_status_string(int status);
+
+/*
+ * exattn_last_cuda_error -- the CUDA call behind the last EXATTN_ERR_CUDA
+ * returned on the calling host thread: "<call>: <cudaError name> (<code>)",
+ * or "<call>: CUresult <code>" for the driver's tensor-map encoder; "" if no
+ * CUDA call of the library has failed on this thread.  Kept per thread, so
+ * it is read on the thread that saw the status.  The text is owned by the
+ * library and stays valid until the thread's next call of this function.
+ */
+const char* exattn_last_cuda_error(void);
 
 /*
  * exattn_device_error -- synchronises the current device, reads and clears

@@ -184,6 +184,33 @@ def test_ex_validation(lib):
     assert bwd(ws_bytes=16) == 6
 
 
+def test_o32_validation(lib):
+    """attn_fwd_o32 / attn_bwd_o32 reject a missing or misaligned fp32 O, and
+    otherwise validate like the _ex calls (fake pointers; nothing launched)."""
+    from exact_attention_67_gb300._lib import Strides
+    P = [0x10000 * (i + 1) for i in range(10)]
+    B, H, N, d = 1, 2, 8, 64
+    good = Strides(H * N * d, N * d, d)
+
+    def fwd(o32=P[5], dt=0, window=0):
+        return lib.attn_fwd_o32(dt, P[0], good, P[1], good, P[2], good, P[3], good, P[4], o32, B, H, N, d, 1,
+                                window, 0.125, None)
+
+    assert fwd(o32=None) == 1
+    assert fwd(o32=P[5] + 4) == 3
+    assert fwd(dt=2) == 4
+    assert fwd(window=-1) == 9
+
+    def bwd(o32=P[3], ws_bytes=1 << 20, scale=0.125):
+        return lib.attn_bwd_o32(0, P[0], good, P[1], good, P[2], good, o32, P[4], good, P[5], P[6], good, P[7],
+                                good, P[8], good, B, H, N, d, 0, 0, scale, P[9], ws_bytes, None)
+
+    assert bwd(o32=None) == 1
+    assert bwd(o32=P[3] + 8) == 3
+    assert bwd(scale=0.0) == 9
+    assert bwd(ws_bytes=16) == 6
+
+
 def test_varlen_validation(lib):
     """attn_fwd_varlen / attn_bwd_varlen reject a missing or misaligned offset
     table and bad sizes before any CUDA call (nothing is launched)."""
