@@ -4,8 +4,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step is one pass of the whole path over one batch of synthetic input:
-attn_fwd (fused forward), then the three backward kernels (row dots D_i,
-dK/dV, dQ).  The default workload is B=1, H=16, N=8192, d=128, causal, bf16
+attn_fwd (fused forward), then the two backward kernels as attn_bwd runs
+them (dQ, which also forms the row terms D_i = dO_i . O_i, then dK/dV).  The default workload is B=1, H=16, N=8192, d=128, causal, bf16
 (the N=8192 causal forward is the case the forward target is stated on).
 Prints ONE JSON line (rank 0).
 
@@ -93,8 +93,7 @@ def load_peaks():
 
 
 def kernel_source_sha(name: str) -> str:
-    src = {"attn_fwd_kernel": "fwd.cu", "bwd_dkdv_kernel": "bwd.cu", "bwd_dq_kernel": "dq.cu",
-           "bwd_rowdot_kernel": "bwd.cu"}[name]
+    src = {"attn_fwd_kernel": "fwd.cu", "bwd_dkdv_kernel": "bwd.cu", "bwd_dq_kernel": "dq.cu"}[name]
     h = hashlib.sha256()
     for f in (src, "ptx.cuh", "kernels.cuh"):
         with open(os.path.join(ROOT, "exact_attention_67_gb300", "csrc", f), "rb") as fh:
@@ -362,25 +361,25 @@ def main():
     causal, scale = w.causal, w.scale
     stream = torch.cuda.current_stream()
     F = w.flops_fwd()
-    kernels = ["attn_fwd_kernel", "bwd_rowdot_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]
+    # The backward as attn_bwd runs it: the dQ kernel also forms the row terms
+    # D_i = dO_i . O_i (stored for dK/dV), then dK/dV.
+    kernels = ["attn_fwd_kernel", "bwd_dq_kernel", "bwd_dkdv_kernel"]
+    nk = len(kernels)
     # algorithmic FLOPs per launch: fwd = 2 GEMMs (QK^T, PV); dK/dV = 4 (S, dP, dV, dK);
-    # dQ = 1 (dQ; its S/dP recomputation is not counted); row dots: bytes only.
+    # dQ = 1 (dQ; its S/dP recomputation and the row dots are not counted).
     alg = {"attn_fwd_kernel": F, "bwd_dkdv_kernel": 2.0 * F, "bwd_dq_kernel": 0.5 * F}
-    nbytes = {"bwd_rowdot_kernel": 2 * 2 * w.B * w.H * w.N * w.d + 4 * w.B * w.H * w.N}
 
     def step(evs):
         evs[0].record(stream)
         ex.attn_fwd(q, k, v, o, lse, causal, scale)
         evs[1].record(stream)
-        ex.attn_bwd_preprocess(o, do, Dws)
+        ex.attn_bwd_d_and_dq(q, k, v, o, do, lse, Dws, dq, causal, scale)
         evs[2].record(stream)
         ex.attn_bwd_dkdv(q, k, v, do, lse, Dws, dk, dv, causal, scale)
         evs[3].record(stream)
-        ex.attn_bwd_dq(q, k, v, do, lse, Dws, dq, causal, scale)
-        evs[4].record(stream)
 
     def new_events(n):
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(n)]
 
     def run_steps(n):
         """n steps, L2 flushed before each (outside its events); per-kernel ms lists."""
@@ -391,7 +390,7 @@ def main():
         return evs
 
     def per_kernel_ms(evs):
-        return [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(4)]
+        return [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(nk)]
 
     evw = run_steps(max(3, args.warmup))
     torch.cuda.synchronize()
@@ -427,7 +426,7 @@ def main():
     reduced = max_over_ranks([sum(per_kernel)] + per_kernel, dev)
     total_ms, per_kernel = reduced[0], reduced[1:]
     rep = per_kernel_ms(ev_rep)
-    rep_steps = [sum(rep[j][i] for j in range(4)) for i in range(n_rep)]
+    rep_steps = [sum(rep[j][i] for j in range(nk)) for i in range(n_rep)]
     med = max_over_ranks([statistics.median(rep_steps)] + [statistics.median(x) for x in rep], dev)
     med_step, med_kernel = med[0], med[1:]
 
@@ -442,14 +441,10 @@ def main():
     for j, (name, ms) in enumerate(zip(kernels, per_kernel)):
         per = ms / steps
         r = {"kernel": name, "ms": per, "median_ms": med_kernel[j], "share": ms / total_ms}
-        if name in alg:
-            r["tflops"] = alg[name] / per / 1e9
-            r["frac_of_peak"] = r["tflops"] / peak
-        else:
-            r["gbs"] = nbytes[name] / per / 1e6
-            r["frac_of_hbm"] = r["gbs"] / peaks["hbm_gbs"] if peaks["hbm_gbs"] else None
+        r["tflops"] = alg[name] / per / 1e9
+        r["frac_of_peak"] = r["tflops"] / peak
         rows.append(r)
-    dom = max(range(4), key=lambda j: per_kernel[j])
+    dom = max(range(nk), key=lambda j: per_kernel[j])
     dname = kernels[dom]
     traffic = dram_traffic(dname, w.name)
     roofline = {"bound": "tensor", "kernel": dname, "achieved": rows[dom].get("tflops"), "peak": peak,
@@ -515,7 +510,7 @@ def main():
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "fwd_pct_peak": 100.0 * fwd_tflops / peak, "fwd_bwd_pct_peak": 100.0 * value / world / peak,
             "median": median, "kernels": rows, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * steps, "clocks": clocks,
+            "gpu_launches": nk * steps, "clocks": clocks,
             "gpu": torch.cuda.get_device_name(dev)}
     print(json.dumps(line), flush=True)
     return 0

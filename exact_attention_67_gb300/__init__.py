@@ -17,14 +17,14 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
+from ._lib import (EXPORTS, ExattnError, Strides, attn_bwd, attn_bwd_d_and_dq, attn_bwd_dkdv, attn_bwd_dq, attn_bwd_ex,
                    attn_bwd_o32, attn_fwd_o32, attn_bwd_preprocess, attn_bwd_varlen, attn_bwd_workspace_size, attn_fwd, attn_fwd_decode, attn_fwd_bwd_host,
                    attn_fwd_bwd_host_workspace_size, attn_fwd_decode_workspace_size, attn_fwd_ex, attn_fwd_varlen,
                    device_error, library_path, load, status_string, version, watchdog_check, watchdog_poll)
 from .host import HostStep, fwd_bwd_from_host
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_o32", "attn_bwd_o32",
+           "attn_bwd_dq", "attn_bwd_d_and_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_o32", "attn_bwd_o32",
            "attn_fwd_varlen", "attn_bwd_varlen", "Strides", "forward", "backward", "forward_varlen", "backward_varlen", "attn_fwd_decode", "attn_fwd_decode_workspace_size",
            "forward_decode", "fwd_bwd_from_host", "HostStep", "attn_fwd_bwd_host",
            "attn_fwd_bwd_host_workspace_size", "attention", "flash_attn_func", "device_error",

@@ -24,7 +24,7 @@ STATUS_NAMES = {
 }
 # Every entry point include/exattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_o32", "attn_bwd_o32", "attn_fwd_varlen",
+           "attn_bwd_dq", "attn_bwd_d_and_dq", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_o32", "attn_bwd_o32", "attn_fwd_varlen",
            "attn_bwd_varlen",
            "attn_fwd_decode_workspace_size", "attn_fwd_decode", "attn_bwd_noalloc",
            "attn_fwd_bwd_host_workspace_size", "attn_fwd_bwd_host",
@@ -76,6 +76,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_dkdv.restype = i
         lib.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.attn_bwd_dq.restype = i
+        lib.attn_bwd_d_and_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.attn_bwd_d_and_dq.restype = i
         lib.exattn_device_error_poll.argtypes = [vp, vp]
         lib.exattn_device_error_poll.restype = i
         S = Strides
@@ -454,6 +456,20 @@ def attn_bwd_dq(q, k, v, dO, lse, D, dq, causal: bool, scale: float, stream=None
     with torch.cuda.device(dev):
         _check(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq), B, H, N, d,
                                   int(bool(causal)), float(scale), _stream(stream, dev)))
+
+
+def attn_bwd_d_and_dq(q, k, v, o, dO, lse, D, dq, causal: bool, scale: float, stream=None) -> None:
+    """C ``attn_bwd_d_and_dq``: D (fp32 [B, H, N], written) and dQ in one kernel."""
+    B, H, N, d = _shape4(q, "q")
+    for n, t in (("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq)):
+        if _shape4(t, n) != (B, H, N, d):
+            raise ValueError(f"{n} shape != q shape")
+    _check_rows(lse, (B, H, N), "lse")
+    _check_rows(D, (B, H, N), "D")
+    dev = _device_of(q, k, v, o, dO, lse, D, dq)
+    with torch.cuda.device(dev):
+        _check(load().attn_bwd_d_and_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq),
+                                        B, H, N, d, int(bool(causal)), float(scale), _stream(stream, dev)))
 
 
 def attn_fwd_bwd_host_workspace_size(B: int, H: int, N: int, d: int, causal: bool) -> int:

@@ -356,7 +356,8 @@ BwdInputs contiguous_inputs(const void* q, const void* k, const void* v, const v
   return BwdInputs{{q, k, v, dO}, {c, c, c, c}};
 }
 
-// The whole backward: D_i, then dK/dV, then dQ, on one stream.
+// The whole backward on one stream: the dQ kernel, which also forms the row
+// terms D_i and stores them in the workspace, then dK/dV, which reads them.
 int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, const Strides& sdo, const float* lse,
              void* dq, const Strides& sdq, void* dk, const Strides& sdk, void* dv, const Strides& sdv, int B, int H,
              int N, int d, int causal, int window, float scale, void* workspace, void* stream,
@@ -378,10 +379,10 @@ int bwd_impl(int dtype, const BwdInputs& in, const void* o, const Strides& so, c
   a.sdv = sdv;
   a.D = static_cast<float*>(workspace);
   a.o32 = o32;
+  a.dq_computes_D = true;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_bwd_prep(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
-  if (launch_bwd_dkdv(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
   if (launch_bwd_dq(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (launch_bwd_dkdv(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
 
@@ -446,6 +447,32 @@ extern "C" int attn_bwd_dq(const void* q, const void* k, const void* v, const vo
   a.D = const_cast<float*>(D);
   a.dq = dq;
   a.sdq = contiguous(H, N, d);
+  return launch_bwd_dq(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+}
+
+extern "C" int attn_bwd_d_and_dq(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                 const float* lse, float* D, void* dq, int B, int H, int N, int d, int causal,
+                                 float scale, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !D || !dq) return EXATTN_ERR_NULL;
+  int rc = check_common(B, H, N, d, scale);
+  if (rc != EXATTN_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(lse, 4) || !aligned(D, 4))
+    return EXATTN_ERR_ALIGN;
+  BwdArgs a{};
+  BwdMaps maps;
+  if ((rc = bwd_setup(a, maps, kBF16, contiguous_inputs(q, k, v, dO, H, N, d), B, H, N, d, causal, scale)) !=
+      EXATTN_OK)
+    return rc;
+  a.o = o;
+  a.so = contiguous(H, N, d);
+  a.dO = dO;
+  a.sdo = a.so;
+  a.lse = lse;
+  a.D = D;
+  a.dq_computes_D = true;
+  a.dq = dq;
+  a.sdq = a.so;
   return launch_bwd_dq(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 

@@ -73,10 +73,10 @@ template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ lse, const float* __restrict__ Dws, T* __restrict__ dq, Strides sdq,
-                  int N_max, int H, int BH, int n_pairs, int group, int window, float scale, float scale_log2,
-                  SeqView seq,
-                  unsigned* err) {
+                  const float* __restrict__ lse, float* __restrict__ Dws, const T* __restrict__ o, Strides so,
+                  const T* __restrict__ dO, Strides sdo, const float* __restrict__ o32, T* __restrict__ dq,
+                  Strides sdq, int N_max, int H, int BH, int n_pairs, int group, int window, float scale,
+                  float scale_log2, SeqView seq, unsigned* err) {
   using C = DqCfg<D>;
   using E = Elem<T>;
   using Bars = DqBars<C::STAGES>;
@@ -294,8 +294,90 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const bool valid = qrow < N;
     // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
     const float neg_lse2 = valid ? -lse[sr0.stat0 + qrow] * kLog2eDq : -INFINITY;
-    const float Drow = valid ? Dws[sr0.stat0 + qrow] : 0.f;
     bool ok = nk_t > 0;
+    float Drow = 0.f;
+    if (ok && (o != nullptr || o32 != nullptr)) {
+      // D_i = sum_c dO_ic O_ic of the warp's 32 rows, computed here and
+      // stored for the dK/dV kernel that runs next.  TPR lanes share a row,
+      // 8 columns (one 16-byte granule) each, in the row-dot kernel's
+      // grouping and order (each lane's 8 products chained by fma from 0,
+      // then a butterfly over the row's lanes), so D is bit-identical to that
+      // kernel's.  A lane's O granules are all requested before the wait for
+      // Q_t, dO_t; dO is then read from its 128-byte-swizzled tile in shared
+      // memory (granule g of row r at g ^ (r mod 8)).
+      constexpr int TPR = D / 8, RPW = 32 / TPR, NI = 32 / RPW;
+      const int sub = lane / TPR, part = lane % TPR;
+      const int pc = part >> 3, pg = part & 7;  // 64-column chunk, granule within it
+      const uint8_t* do_tile = smem + C::OFF_DO + t * C::QTILE + pc * C::QCHUNK;
+      // Sum over the row's lanes; row i * RPW + s of the warp's 32 belongs to
+      // lane i * RPW + s and its sum sits in lanes s * TPR ... s * TPR + TPR - 1.
+      auto finish = [&](int i, float a) {
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+#pragma unroll
+        for (int s2 = 0; s2 < RPW; ++s2) {
+          const float v = __shfl_sync(0xffffffffu, a, s2 * TPR);
+          if (lane == i * RPW + s2) Drow = v;
+        }
+      };
+      if (o32 == nullptr) {
+        float acc[NI];
+        uint4 oa[NI];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const int rr = tile_r0 + wq * 32 + i * RPW + sub;
+          oa[i] = rr < N ? __ldg(reinterpret_cast<const uint4*>(
+                               o + bt * so.b + hh * so.h + static_cast<long long>(row0 + rr) * so.n) + part)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+        ok = mbar_wait(&bars->qd_full[t], 0, wc);
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const int r = wq * 32 + i * RPW + sub;  // row within the tile
+          acc[i] = 0.f;
+          if (ok && tile_r0 + r < N) {
+            const uint4 c = *reinterpret_cast<const uint4*>(do_tile + r * 128 + ((pg ^ (r & 7)) << 4));
+            const uint32_t* a2 = reinterpret_cast<const uint32_t*>(&oa[i]);
+            const uint32_t* c2 = reinterpret_cast<const uint32_t*>(&c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 fa = E::unpack(a2[e]);
+              const float2 fc = E::unpack(c2[e]);
+              acc[i] = fmaf(fa.x, fc.x, acc[i]);
+              acc[i] = fmaf(fa.y, fc.y, acc[i]);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < NI; ++i) finish(i, acc[i]);
+      } else {
+        // fp32 O, contiguous [B*H, N, d] rows (fixed-length calls only).
+        ok = mbar_wait(&bars->qd_full[t], 0, wc);
+#pragma unroll 4
+        for (int i = 0; i < NI; ++i) {
+          const int r = wq * 32 + i * RPW + sub;
+          float acc = 0.f;
+          if (ok && tile_r0 + r < N) {
+            const float4* o4 =
+                reinterpret_cast<const float4*>(o32 + (static_cast<long long>(bh) * N + tile_r0 + r) * D) + 2 * part;
+            const float4 a0 = __ldg(o4), a1 = __ldg(o4 + 1);
+            const float fa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint4 c = *reinterpret_cast<const uint4*>(do_tile + r * 128 + ((pg ^ (r & 7)) << 4));
+            const uint32_t* c2 = reinterpret_cast<const uint32_t*>(&c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 fc = E::unpack(c2[e]);
+              acc = fmaf(fa[2 * e], fc.x, acc);
+              acc = fmaf(fa[2 * e + 1], fc.y, acc);
+            }
+          }
+          finish(i, acc);
+        }
+      }
+      if (ok && valid) Dws[sr0.stat0 + qrow] = Drow;
+    } else if (valid) {
+      Drow = Dws[sr0.stat0 + qrow];
+    }
     for (int it = 0; ok && it < nk_t; ++it) {
       if (!(ok = mbar_wait(&bars->s_full[t], it & 1, wc))) break;
       if (row == 0) EXATTN_TRACE_POINT(2 + t, it, 0);
@@ -389,9 +471,13 @@ static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   // K, V of a group's heads fill a quarter of L2 (B4 H32 N4096 d64: 612-743 MB
   // per launch with half of L2, 327 MB with a quarter; 339.7 MB algorithmic).
   const int group = l2_group(2ll * a.N * D * static_cast<long long>(sizeof(T)), a.BH, kL2GroupBytes / 2);
+  // With a.dq_computes_D the kernel forms D_i from O (or the fp32 copy) and
+  // dO and writes it to a.D; otherwise it reads a.D.
+  const T* o = a.dq_computes_D ? static_cast<const T*>(a.o) : nullptr;
+  const float* o32 = a.dq_computes_D ? a.o32 : nullptr;
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, static_cast<T*>(a.dq), a.sdq, a.N, a.H,
-      a.BH, n_pairs, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
+      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, o, a.so, static_cast<const T*>(a.dO), a.sdo, o32,
+      static_cast<T*>(a.dq), a.sdq, a.N, a.H, a.BH, n_pairs, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return note_cuda(cudaGetLastError(), "dQ kernel launch");
 }
 

@@ -150,6 +150,7 @@ struct BwdArgs {
   const float* lse;         // fp32 [B*H, N], natural log
   float* D;                 // workspace: fp32 [B*H, N]
   const float* o32;         // optional fp32 O, contiguous [B*H, N, d]: D_i from it instead of o
+  bool dq_computes_D;       // the dQ kernel forms D_i (from o or o32, and dO) and writes it to D
   int N, H, BH, d, causal, dtype;
   int window;               // as FwdArgs::window
   SeqView seq;              // as FwdArgs::seq

@@ -70,7 +70,9 @@ typedef enum {
  *   scale   : multiplies Q K^T before masking and softmax (1/sqrt(d) usual).
  *   stream  : cudaStream_t.
  * Arithmetic: bf16 products accumulated in fp32 on the tensor cores; the
- * softmax runs in fp32; P is rounded to bf16 before the P V product.
+ * softmax runs in fp32; P is rounded to f16 before the P V product, and V
+ * is converted to f16 in shared memory for it (exact for 2^-14 <= |v| <=
+ * 65504 and for 0; entries beyond +-65504 are not supported).
  * Returns an exattn_status.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -93,7 +95,9 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d, int causal);
  *                     attn_bwd_workspace_size(B, H, N, d, causal) bytes,
  *                     16-byte aligned, owned by the caller; its contents on
  *                     entry are ignored and on return are unspecified.
- * It computes D_i = sum_c dO_ic O_ic, then for every tile pair recomputes
+ * It computes D_i = sum_c dO_ic O_ic (inside the dQ kernel, which stores it
+ * in the workspace for the dK/dV kernel that follows), and for every tile
+ * pair recomputes
  * P_ij = exp(scale q_i.k_j - lse_i), dP_ij = dO_i.v_j, dS_ij = P_ij (dP_ij - D_i)
  * and accumulates dV_j += P_ij dO_i, dK_j += scale dS_ij q_i (one pass over
  * query tiles per key tile) and dQ_i += scale dS_ij k_j (one pass over key
@@ -106,10 +110,12 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              size_t workspace_bytes, void* stream);
 
 /*
- * The three stages of attn_bwd as separate calls, for callers that schedule
- * them themselves (e.g. dK/dV and dQ on two streams once D is ready, or
- * timing each kernel).  attn_bwd(...) equals attn_bwd_preprocess followed by
- * attn_bwd_dkdv and attn_bwd_dq on one stream, with D in the workspace.
+ * The stages of attn_bwd as separate calls, for callers that schedule them
+ * themselves (e.g. dK/dV and dQ on two streams once D is ready, or timing
+ * each kernel).  attn_bwd(...) equals attn_bwd_d_and_dq followed by
+ * attn_bwd_dkdv on one stream, with D in the workspace; attn_bwd_preprocess
+ * followed by attn_bwd_dkdv and attn_bwd_dq gives bit-identical results
+ * with one more launch.
  *
  * attn_bwd_preprocess -- D[b,h,i] = sum_c dO[b,h,i,c] O[b,h,i,c], the
  *   per-row term of the softmax gradient (dS_ij = P_ij (dP_ij - D_i)).
@@ -117,6 +123,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  * attn_bwd_dkdv -- dK and dV (bf16 [B, H, N, d], written) from q, k, v, dO,
  *   lse (as written by attn_fwd) and D (from attn_bwd_preprocess).
  * attn_bwd_dq   -- dQ (bf16 [B, H, N, d], written) from the same inputs.
+ * attn_bwd_d_and_dq -- both D (written, as attn_bwd_preprocess writes it,
+ *   bit for bit) and dQ (as attn_bwd_dq computes it from that D) in one
+ *   kernel, from q, k, v, o, dO and lse; D is complete when the call's work
+ *   on the stream is.
  * Validation, alignment and error codes as for attn_bwd.
  */
 int attn_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d, void* stream);
@@ -124,6 +134,8 @@ int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, c
                   void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
 int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* D,
                 void* dq, int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_d_and_dq(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      float* D, void* dq, int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
  * Element type and layout for the _ex calls below.  The flash_attn_func

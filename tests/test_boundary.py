@@ -142,6 +142,19 @@ def test_stage_validation(lib):
     assert lib.attn_bwd_dq(*args[:6], None, 1, 1, 8, 64, 0, 0.1, None) == 1
     assert lib.attn_bwd_dq(*args, 1, 1, 8, 128, 1, float("inf"), None) == 9
     assert lib.attn_bwd_dq(*args, -1, 1, 8, 128, 1, 0.1, None) == 2
+    # attn_bwd_d_and_dq(q, k, v, o, dO, lse, D, dq, B, H, N, d, causal, scale, stream)
+    args = list(P[:8])
+    for i in range(8):
+        nul = list(args)
+        nul[i] = None
+        assert lib.attn_bwd_d_and_dq(*nul, 1, 1, 8, 64, 0, 0.1, None) == 1
+    assert lib.attn_bwd_d_and_dq(*args, 1, 1, 8, 64, 0, float("nan"), None) == 9
+    assert lib.attn_bwd_d_and_dq(*args, 1, 1, 8, 96, 0, 0.1, None) == 4
+    assert lib.attn_bwd_d_and_dq(*args, 1, 0, 8, 64, 0, 0.1, None) == 2
+    for i, off in ((3, 8), (4, 8), (6, 2), (7, 8)):  # o, dO, D, dq misaligned
+        bad = list(args)
+        bad[i] += off
+        assert lib.attn_bwd_d_and_dq(*bad, 1, 1, 8, 64, 0, 0.1, None) == 3
 
 
 def test_ex_validation(lib):
