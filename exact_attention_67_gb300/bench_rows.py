@@ -7,7 +7,9 @@ window, a packed variable-length batch and decode-shaped forwards.  Inputs are
 seeded synthetic bf16/f16 N(0, 1), resident on the device; each figure is the
 mean device time of ``iters`` back-to-back calls between two CUDA events after
 three warm-up calls (the square cases move far more than L2 per call and are
-compute-bound; the decode cases read more K/V than L2 holds).  FLOPs count
+compute-bound); the decode cases run the C ABI call on preallocated buffers,
+``iters`` calls captured once as a CUDA graph and replayed, so that the
+host's per-call work does not show in calls of a few microseconds.  FLOPs count
 only visible (query, key) pairs: 4 d per pair forward, 2.5x that backward.
 """
 from __future__ import annotations
@@ -18,7 +20,7 @@ import os
 
 import torch
 
-from . import attn_fwd_decode_workspace_size, backward, backward_varlen, forward, forward_decode, forward_varlen
+from . import attn_fwd_decode, attn_fwd_decode_workspace_size, backward, backward_varlen, forward, forward_varlen
 from .synth import seeded_bf16
 
 DEV = torch.device("cuda:0")
@@ -91,11 +93,39 @@ def _varlen(name, lens, H, d, causal, dtype, iters, peak):
             "fwd_bwd_tflops": 3.5 * f / (t_f + t_b) / 1e9, "fwd_pct_peak": f / t_f / 1e9 / peak * 100}
 
 
+def _time_graph_ms(fn, iters: int) -> float:
+    """Mean device time of ``iters`` calls captured once as a CUDA graph and
+    replayed: back-to-back launches with no host work between them, for
+    calls too short to hide the host's per-call overhead."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(iters):
+            fn()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / iters
+
+
 def _decode(name, B, H, Nq, Nk, d, iters, hbm):
     q = seeded_bf16((B, H, Nq, d), 31, 1.0).to(DEV)
     k = seeded_bf16((B, H, Nk, d), 32, 1.0).to(DEV)
     v = seeded_bf16((B, H, Nk, d), 33, 1.0).to(DEV)
-    t = _time_ms(lambda: forward_decode(q, k, v, True, d ** -0.5), iters)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=DEV)
+    nws = attn_fwd_decode_workspace_size(B, H, Nq, Nk, d)
+    ws = torch.empty(nws, dtype=torch.uint8, device=DEV) if nws else None
+    # The C ABI call on preallocated buffers (what forward_decode runs, minus
+    # its allocations and watchdog poll), replayed from a CUDA graph.
+    t = _time_graph_ms(lambda: attn_fwd_decode(q, k, v, o, lse, True, d ** -0.5, ws), iters)
     nbytes = 2.0 * B * H * Nk * d * 2 + 2.0 * B * H * Nq * d * 2  # K, V read; Q read, O written
     return {"case": name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": True, "ms": t,
             "gbs": nbytes / t / 1e6, "pct_hbm": nbytes / t / 1e6 / hbm * 100,
