@@ -307,7 +307,7 @@ namespace {
 // device state, the tensor maps of the given inputs (a null input skips its
 // maps), and the launch arguments.
 struct BwdMaps {
-  CUtensorMap m[8];
+  CUtensorMap m[10];  // 128-row boxes of q, k, v, dO; 64-row boxes; k, v in the dQ kernel's key steps (d = 64)
 };
 
 struct BwdInputs {
@@ -328,6 +328,14 @@ int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, 
         !make_map(&maps.m[4 + i], in.p[i], dtype, map_b, H, map_n, d, in.s[i], 64))
       return EXATTN_ERR_CUDA;
   }
+  const int kstep = dq_key_step(d);
+  const bool own_kv_maps = kstep != 64 && kstep != 128;
+  for (int i = 1; own_kv_maps && i < 3; ++i) {
+    if (in.p[i] && !make_map(&maps.m[7 + i], in.p[i], dtype, map_b, H, map_n, d, in.s[i], kstep))
+      return EXATTN_ERR_CUDA;
+  }
+  a.tm_kdq = own_kv_maps ? &maps.m[8] : (kstep == 64 ? &maps.m[5] : &maps.m[1]);
+  a.tm_vdq = own_kv_maps ? &maps.m[9] : (kstep == 64 ? &maps.m[6] : &maps.m[2]);
   a.tm_q128 = &maps.m[0];
   a.tm_k128 = &maps.m[1];
   a.tm_v128 = &maps.m[2];

@@ -9,8 +9,8 @@
 // GB300 mapping (one CTA per SM, 352 threads), the same ping-pong as the
 // forward kernel:
 //   * the CTA owns two 128-row query tiles of one (batch, head); Q and dO of
-//     both stay in shared memory, 64-key tiles of K and V stream through a
-//     TMA ring that both query tiles share;
+//     both stay in shared memory, key tiles of K and V (64 keys at d = 128,
+//     96 at d = 64) stream through a TMA ring that both query tiles share;
 //   * warp 9 + t issues the MMAs of query tile t (warp-uniform loop, elected
 //     lane): per key step, dQ_t += dS_t K_j with dS_t read from TMEM, then
 //     S_t = Q_t K_j+1^T and dP_t = dO_t V_j+1^T into TMEM.  With one issuer
@@ -21,7 +21,8 @@
 //     tensor core runs the other tile's MMAs, which hides the hand-off
 //     latency between the two roles;
 //   * warp 8 issues the TMA loads.
-// TMEM per tile t (base 256 t): dQ_t [0,128), S_t [128,192), dP_t [192,256).
+// TMEM per tile t (base 256 t): d = 128: dQ_t [0,128), S_t [128,192), dP_t
+// [192,256); d = 64: dQ_t [0,64), S_t [64,160), dP_t [160,256).
 // Causal: key tiles above the diagonal are skipped per query tile, diagonal
 // tiles masked per element (key j visible to query i iff j <= i).
 #include "kernels.cuh"
@@ -36,7 +37,7 @@ constexpr float kLog2eDq = 1.4426950408889634f;
 template <int D>
 struct DqCfg {
   static constexpr int BM = 128;  // queries per tile (TMEM lanes); two tiles per CTA
-  static constexpr int BN = 64;   // keys per step
+  static constexpr int BN = dq_key_step(D);  // keys per step: 64 at d = 128, 96 at d = 64
   static constexpr int NCHUNK = D / 64;
   static constexpr int QCHUNK = BM * 128;
   static constexpr int KCHUNK = BN * 128;
@@ -51,7 +52,10 @@ struct DqCfg {
   static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
   static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit");
   static constexpr int THREADS = 352;  // warps 0-7 elementwise (two tiles), 8 producer, 9-10 MMA
-  static constexpr uint32_t TM_TILE = 256, TM_DQ = 0, TM_S = 128, TM_DP = 192, TM_COLS = 512;
+  // TMEM per tile t (base 256 t): dQ_t, then S_t and dP_t of BN columns each.
+  static constexpr uint32_t TM_TILE = 256, TM_DQ = 0, TM_S = D == 64 ? 64 : 128, TM_DP = TM_S + BN, TM_COLS = 512;
+  static_assert(TM_DQ + D <= TM_S && TM_DP + BN <= TM_TILE, "a tile's dQ, S, dP exceed its 256 TMEM columns");
+  static_assert(BN == 64 || BN == 96, "the elementwise step handles two or three 32-column chunks");
 };
 
 template <int STAGES>
@@ -382,49 +386,70 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       if (!(ok = mbar_wait(&bars->s_full[t], it & 1, wc))) break;
       if (row == 0) EXATTN_TRACE_POINT(2 + t, it, 0);
       tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tbase + C::TM_S, sr[0]);
-      tmem_ld32(tbase + C::TM_S + 32, sr[1]);
-      tmem_ld32(tbase + C::TM_DP, dr[0]);
-      tmem_ld32(tbase + C::TM_DP + 32, dr[1]);
+      uint32_t sa[32], da[32], sb[32], db[32];
+      tmem_ld32(tbase + C::TM_S, sa);
+      tmem_ld32(tbase + C::TM_S + 32, sb);
+      tmem_ld32(tbase + C::TM_DP, da);
+      tmem_ld32(tbase + C::TM_DP + 32, db);
       tmem_wait_ld();
-      tmem_reg_fence(sr[0]);
-      tmem_reg_fence(sr[1]);
-      tmem_reg_fence(dr[0]);
-      tmem_reg_fence(dr[1]);
+      tmem_reg_fence(sa);
+      tmem_reg_fence(sb);
+      tmem_reg_fence(da);
+      tmem_reg_fence(db);
       const int kj0 = (kv_lo + it) * C::BN;
       const bool need_mask = (CAUSAL && kj0 + C::BN - 1 > tile_r0) || (kj0 + C::BN > N) ||
                              (window > 0 && (kj0 < tile_r0 + C::BM - window ||
                                              (!CAUSAL && kj0 + C::BN - 1 > tile_r0 + window - 1)));
+      // Hidden scores become -inf, so P = 0 and dS = 0 there: key column c
+      // is visible to this row iff lo <= c < lim.
+      int lim = C::BN, lo = 0;
       if (need_mask) {
-        // Hidden scores become -inf, so P = 0 and dS = 0 there: key column c
-        // is visible to this row iff lo <= c < lim.
-        int lim = N - kj0;
+        lim = N - kj0;
         if (CAUSAL) lim = min(lim, qrow - kj0 + 1);
         else if (window > 0) lim = min(lim, qrow + window - kj0);
-        const int lo = window > 0 ? qrow - window + 1 - kj0 : 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (h * 32 + e >= lim || h * 32 + e < lo) sr[h][e] = __float_as_uint(-INFINITY);
+        lo = window > 0 ? qrow - window + 1 - kj0 : 0;
       }
       const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(neg_lse2, neg_lse2);
       const float2 nD2 = make_float2(-Drow, -Drow);
+      auto mask = [&](int h, uint32_t (&sv)[32]) {
+        if (need_mask) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+          for (int e = 0; e < 32; ++e)
+            if (h * 32 + e >= lim || h * 32 + e < lo) sv[e] = __float_as_uint(-INFINITY);
+        }
+      };
+      // dS of 32 key columns (chunk h of S and dP, in registers), written as
+      // 16 packed columns over the first half of S: chunk h's output lands on
+      // columns of chunks already read.
+      auto chunk = [&](int h, const uint32_t (&sv)[32], const uint32_t (&dv)[32]) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           // Packed fp32 pairs: one instruction per two columns.
-          const float2 y = ffma2(make_float2(__uint_as_float(sr[h][2 * e]), __uint_as_float(sr[h][2 * e + 1])),
-                                 sc2, nl2);
+          const float2 y = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sc2, nl2);
           const float2 p = make_float2(ex2(y.x), ex2(y.y));
-          const float2 dsv = fmul2(p, fadd2(make_float2(__uint_as_float(dr[h][2 * e]),
-                                                        __uint_as_float(dr[h][2 * e + 1])), nD2));
+          const float2 dsv =
+              fmul2(p, fadd2(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nD2));
           pk[e] = E::pack(dsv.x, dsv.y);
         }
-        tmem_st16(tbase + C::TM_S + h * 16, pk);  // dS over the first 32 columns of S
+        tmem_st16(tbase + C::TM_S + h * 16, pk);
+      };
+      mask(0, sa);
+      mask(1, sb);
+      chunk(0, sa, da);
+      if constexpr (C::BN == 96) {
+        // A third chunk, loaded into chunk 0's registers once those are
+        // consumed, under chunk 1's math.
+        tmem_ld32(tbase + C::TM_S + 64, sa);
+        tmem_ld32(tbase + C::TM_DP + 64, da);
+      }
+      chunk(1, sb, db);
+      if constexpr (C::BN == 96) {
+        tmem_wait_ld();
+        tmem_reg_fence(sa);
+        tmem_reg_fence(da);
+        mask(2, sa);
+        chunk(2, sa, da);
       }
       tmem_wait_st();
       if (lane == 0) EXATTN_TRACE_POINT(2 + t, it, 1 + wq);
@@ -476,7 +501,7 @@ static cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t stream) {
   const T* o = a.dq_computes_D ? static_cast<const T*>(a.o) : nullptr;
   const float* o32 = a.dq_computes_D ? a.o32 : nullptr;
   kern<<<static_cast<unsigned>(static_cast<long long>(n_pairs) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q128, *a.tm_k64, *a.tm_v64, *a.tm_do128, a.lse, a.D, o, a.so, static_cast<const T*>(a.dO), a.sdo, o32,
+      *a.tm_q128, *a.tm_kdq, *a.tm_vdq, *a.tm_do128, a.lse, a.D, o, a.so, static_cast<const T*>(a.dO), a.sdo, o32,
       static_cast<T*>(a.dq), a.sdq, a.N, a.H, a.BH, n_pairs, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return note_cuda(cudaGetLastError(), "dQ kernel launch");
 }

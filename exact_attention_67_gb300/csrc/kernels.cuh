@@ -83,6 +83,11 @@ __host__ __device__ __forceinline__ GridPos grid_pos(int block, int BH, int n_ti
   return p;
 }
 
+// Keys per step of the dQ kernel: 64 at d = 128; 96 at d = 64, where a
+// query tile's TMEM (dQ 64 + S 96 + dP 96 columns) still fits two tiles in
+// 512 columns and each step's fixed hand-off latencies cover more keys.
+constexpr int dq_key_step(int d) { return d == 64 ? 96 : 64; }
+
 // Problems per group for grid_pos: as many as keep their re-read operands
 // (bytes_per_problem each) within `budget` bytes of the 129 MB L2 (half of
 // it by default), at least one.
@@ -137,6 +142,9 @@ struct BwdArgs {
   const CUtensorMap* tm_k64;
   const CUtensorMap* tm_v64;
   const CUtensorMap* tm_do64;
+  // K and V with a box of dq_key_step(d) rows: the dQ kernel's key tiles
+  const CUtensorMap* tm_kdq;
+  const CUtensorMap* tm_vdq;
   const void* o;            // [B, H, N, d] views (d contiguous) with their element strides
   Strides so;
   const void* dO;
