@@ -307,7 +307,9 @@ namespace {
 // device state, the tensor maps of the given inputs (a null input skips its
 // maps), and the launch arguments.
 struct BwdMaps {
-  CUtensorMap m[10];  // 128-row boxes of q, k, v, dO; 64-row boxes; k, v in the dQ kernel's key steps (d = 64)
+  // 128-row boxes of q, k, v, dO; 64-row boxes; k, v in the dQ kernel's key
+  // steps and q, dO in the dK/dV kernel's query steps where those are 96.
+  CUtensorMap m[12];
 };
 
 struct BwdInputs {
@@ -336,6 +338,14 @@ int bwd_setup(BwdArgs& a, BwdMaps& maps, int dtype, const BwdInputs& in, int B, 
   }
   a.tm_kdq = own_kv_maps ? &maps.m[8] : (kstep == 64 ? &maps.m[5] : &maps.m[1]);
   a.tm_vdq = own_kv_maps ? &maps.m[9] : (kstep == 64 ? &maps.m[6] : &maps.m[2]);
+  const int qstep = dkdv_query_step(d);
+  const bool own_q_maps = qstep != 64 && qstep != 128;
+  for (int i = 0; own_q_maps && i < 4; i += 3) {  // q and dO
+    if (in.p[i] && !make_map(&maps.m[i == 0 ? 10 : 11], in.p[i], dtype, map_b, H, map_n, d, in.s[i], qstep))
+      return EXATTN_ERR_CUDA;
+  }
+  a.tm_qkv = own_q_maps ? &maps.m[10] : (qstep == 64 ? &maps.m[4] : &maps.m[0]);
+  a.tm_dokv = own_q_maps ? &maps.m[11] : (qstep == 64 ? &maps.m[7] : &maps.m[3]);
   a.tm_q128 = &maps.m[0];
   a.tm_k128 = &maps.m[1];
   a.tm_v128 = &maps.m[2];

@@ -8,16 +8,19 @@
 //
 // Three kernels, no atomics (every output element is summed by one CTA in a
 // fixed order, so results are bit-identical run to run):
-//   1. bwd_rowdot_kernel: D_i = sum_c dO_ic O_ic (bandwidth bound).
-//   2. bwd_dkdv_kernel: one CTA per 128-key tile; streams 64-query tiles of
-//      Q and dO (TMA ring); per tile the tensor core computes S^T = K Q_i^T
-//      and dP^T = V dO_i^T into TMEM, a warpgroup (thread = key row; two at
-//      d = 64, each on half the query columns) turns them into P^T and dS^T
+//   1. bwd_rowdot_kernel: D_i = sum_c dO_ic O_ic (bandwidth bound; the
+//      separate attn_bwd_preprocess call -- attn_bwd forms D_i inside the
+//      dQ kernel).
+//   2. bwd_dkdv_kernel: one CTA per 128-key tile; streams query tiles (64
+//      queries at d = 128, 96 at d = 64) of Q and dO (TMA ring); per tile
+//      the tensor core computes S^T = K Q_i^T and dP^T = V dO_i^T into TMEM,
+//      warpgroups (thread = key row; one at d = 128, three at d = 64, each
+//      on 32 of the step's query columns) turn them into P^T and dS^T
 //      (input type, written back over S^T and dP^T), and the
 //      tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
 //      S^T/dP^T are double buffered so the next tile's products overlap the
 //      current elementwise work.
-//   3. bwd_dq_kernel (dq.cu): two 128-query tiles per CTA; streams 64-key
+//   3. bwd_dq_kernel (dq.cu): two 128-query tiles per CTA; streams key
 //      tiles of K and V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (input
 //      type) written back, and dQ += dS K_j accumulated in TMEM.
 // Causal: key tiles wholly above the diagonal are skipped, diagonal tiles are
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o
 template <int D>
 struct DkdvCfg {
   static constexpr int BM = 128;  // keys per CTA (TMEM lanes)
-  static constexpr int BR = 64;   // queries per step
+  static constexpr int BR = dkdv_query_step(D);  // queries per step: 64 at d = 128, 96 at d = 64
   static constexpr int NCHUNK = D / 64;
   static constexpr int KCHUNK = BM * 128;  // bytes of one 64-column chunk of a 128-row tile
   static constexpr int QCHUNK = BR * 128;  // ... of a 64-row tile
@@ -104,14 +107,16 @@ struct DkdvCfg {
   static constexpr int OFF_BAR = OFF_STAT + STAGES * 2 * BR * 4;
   // At least 120 KB so that only one CTA (which holds all 512 TMEM columns) fits on an SM.
   static constexpr int SMEM_BYTES = (OFF_BAR + 512 + 1024 > 120 * 1024) ? OFF_BAR + 512 + 1024 : 120 * 1024;
+  static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit");
   // Elementwise warps: EW_GROUPS groups of four, one warp per TMEM lane
-  // quarter in each group, group g taking query columns 64 g / EW_GROUPS
+  // quarter in each group, group g taking query columns BR g / EW_GROUPS
   // onwards of the step.  At d = 64 a step's MMA chain is half as long as at
-  // d = 128 while the softmax work is the same, so two groups halve the
-  // hand-off latency that bounds it; at d = 128 the chain hides one group's
-  // latency and the second costs registers.  Then the producer warp, then the
-  // MMA warp.
-  static constexpr int EW_GROUPS = D == 64 ? 2 : 1;
+  // d = 128 while the softmax work is the same, so one group per 32-column
+  // chunk (three for the 96-query steps) divides the hand-off latency that
+  // bounds it; at d = 128 the chain hides one group's latency and a second
+  // costs registers.  Then the producer warp, then the MMA warp.
+  static constexpr int QCH = BR / 32;  // 32-column query chunks per step
+  static constexpr int EW_GROUPS = D == 64 ? QCH : 1;
   static constexpr int EW_WARPS = 4 * EW_GROUPS;
   static constexpr int PRODUCER_WARP = EW_WARPS, MMA_WARP = EW_WARPS + 1;
   static constexpr int THREADS = 32 * (EW_WARPS + 2);
@@ -126,7 +131,11 @@ struct DkdvCfg {
   // Q/dO stage released right after the step's own dV, dK MMAs (d = 64), or
   // inside the next block of score MMAs (d = 128).
   static constexpr bool EARLY_RELEASE = D == 64;
-  static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_BUF = 256, TM_COLS = 512;  // buffer b: S^T at +128b, dP^T at +128b+64
+  // TMEM: dK, dV (D columns each), then two buffers of S^T and dP^T (BR
+  // columns each): buffer b's S^T at TM_BUF + 2 BR b, its dP^T BR further.
+  static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_BUF = 2 * D, TM_COLS = 512;
+  static_assert(TM_BUF + 4 * BR <= TM_COLS, "dK, dV and two S^T/dP^T buffers exceed TMEM");
+  static_assert(QCH % EW_GROUPS == 0, "each elementwise group takes whole 32-column chunks");
 };
 
 template <int STAGES>
@@ -222,10 +231,10 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     }
     // Row terms of the next step are fetched into registers one step ahead, so
     // their global-load latency overlaps the wait for a free stage.
-    auto fetch_terms = [&](int it, float (&l2)[2], float (&dd)[2]) {
+    auto fetch_terms = [&](int it, float (&l2)[C::QCH], float (&dd)[C::QCH]) {
       const int qi0 = (i_begin + it) * C::BR;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < C::QCH; ++u) {
         const int qi = qi0 + lane + 32 * u;
         const bool valid = it < nq && qi < N;
         // Rows past N (zero-filled by TMA) get P = 0 and D = 0: no contribution.
@@ -233,13 +242,18 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         dd[u] = valid ? Dws[sr0.stat0 + qi] : 0.f;
       }
     };
-    float nl2[2], ndd[2];
+    float nl2[C::QCH], ndd[C::QCH];
     fetch_terms(0, nl2, ndd);
     int issued = 0;
     for (int it = 0; it < nq; ++it) {
       const int s = it % C::STAGES;
       const uint32_t ph = (it / C::STAGES) & 1;
-      const float l2a = nl2[0], l2b = nl2[1], dda = ndd[0], ddb = ndd[1];
+      float l2c[C::QCH], ddc[C::QCH];
+#pragma unroll
+      for (int u = 0; u < C::QCH; ++u) {
+        l2c[u] = nl2[u];
+        ddc[u] = ndd[u];
+      }
       fetch_terms(it + 1, nl2, ndd);
       if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
       if (lane == 0) EXATTN_TRACE_POINT(0, it, 0);
@@ -247,10 +261,11 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       float* st_lse2 = stat + s * 2 * C::BR;
       float* st_D = st_lse2 + C::BR;
       // Stored negated, so the elementwise warps add them.
-      st_lse2[lane] = -l2a;
-      st_lse2[lane + 32] = -l2b;
-      st_D[lane] = -dda;
-      st_D[lane + 32] = -ddb;
+#pragma unroll
+      for (int u = 0; u < C::QCH; ++u) {
+        st_lse2[lane + 32 * u] = -l2c[u];
+        st_D[lane + 32 * u] = -ddc[u];
+      }
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::QTILE);
@@ -289,8 +304,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       for (int kk = kk0; kk < kk1; ++kk) {
         const uint32_t ko = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
         const uint32_t qo = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + C::TM_BUF + b * 128, k_desc + ko, qa + qo, idesc_s, kk > 0);
-        mma_ss(tmem + C::TM_BUF + b * 128 + 64, v_desc + ko, da + qo, idesc_s, kk > 0);
+        mma_ss(tmem + C::TM_BUF + b * 2 * C::BR, k_desc + ko, qa + qo, idesc_s, kk > 0);
+        mma_ss(tmem + C::TM_BUF + b * 2 * C::BR + C::BR, v_desc + ko, da + qo, idesc_s, kk > 0);
       }
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -339,9 +354,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
           // P^T (dS^T) sit at column P_STRIDE (kk / 2) + 8 (kk % 2) of S^T (dP^T).
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           const uint32_t col = (kk >> 1) * C::P_STRIDE + (kk & 1) * 8;
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_BUF + b * 128 + col, da + ((kk * 16 * 128) >> 4), idesc_acc, acc);
-          mma_ts(tmem + C::TM_DK, tmem + C::TM_BUF + b * 128 + 64 + col, qa + ((kk * 16 * 128) >> 4), idesc_acc,
-                 acc);
+          const uint32_t buf = tmem + C::TM_BUF + b * 2 * C::BR;
+          mma_ts(tmem + C::TM_DV, buf + col, da + ((kk * 16 * 128) >> 4), idesc_acc, acc);
+          mma_ts(tmem + C::TM_DK, buf + C::BR + col, qa + ((kk * 16 * 128) >> 4), idesc_acc, acc);
         }
         if (C::EARLY_RELEASE) {
           mma_commit(&bars->st_empty[s]);
@@ -363,8 +378,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ elementwise (thread = key row)
     // Warp w takes TMEM lane quarter w % 4 and the 32-column chunks
-    // NC (w / 4) .. NC (w / 4) + NC - 1 of the step's 64 query columns.
-    constexpr int NC = 2 / C::EW_GROUPS;
+    // NC (w / 4) .. NC (w / 4) + NC - 1 of the step's BR query columns.
+    constexpr int NC = C::QCH / C::EW_GROUPS;
     const int wq = warp & 3, group = C::EW_GROUPS == 1 ? 0 : warp >> 2;
     const int row = wq * 32 + lane;
     const int key = k0 + row;
@@ -378,12 +393,12 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       if (!(ok = mbar_wait(&bars->st_full[s], (it / C::STAGES) & 1, wc))) break;
       if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 1);
       tc_fence_after();
-      const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 128;
+      const uint32_t tb = tmem + lane_bits + C::TM_BUF + b * 2 * C::BR;
       uint32_t sr[NC][32], dr[NC][32];
 #pragma unroll
       for (int g = 0; g < NC; ++g) {
         tmem_ld32(tb + 32 * (group * NC + g), sr[g]);
-        tmem_ld32(tb + 64 + 32 * (group * NC + g), dr[g]);
+        tmem_ld32(tb + C::BR + 32 * (group * NC + g), dr[g]);
       }
       tmem_wait_ld();
 #pragma unroll
@@ -439,9 +454,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
           dk_[2 * q4 + 1] = E::pack(dsv[2], dsv[3]);
         }
         // P^T of queries 32 ch .. 32 ch + 31 at columns P_STRIDE ch onwards,
-        // dS^T 64 columns further.
+        // dS^T BR columns further.
         tmem_st16(tb + ch * C::P_STRIDE, pk);
-        tmem_st16(tb + 64 + ch * C::P_STRIDE, dk_);
+        tmem_st16(tb + C::BR + ch * C::P_STRIDE, dk_);
       }
       tmem_wait_st();
       if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 3);
@@ -540,7 +555,7 @@ static cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   // N16384 d128 unchanged within 0.5 %).
   const int group = l2_group(2ll * a.N * D * static_cast<long long>(sizeof(T)), a.BH, kL2GroupBytes / 2);
   kern<<<static_cast<unsigned>(static_cast<long long>(n_kt) * a.BH), C::THREADS, C::SMEM_BYTES, stream>>>(
-      *a.tm_q64, *a.tm_k128, *a.tm_v128, *a.tm_do64, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
+      *a.tm_qkv, *a.tm_k128, *a.tm_v128, *a.tm_dokv, a.lse, a.D, static_cast<T*>(a.dk), a.sdk,
       static_cast<T*>(a.dv), a.sdv, a.N, a.H, a.BH, n_kt, group, a.window, a.scale, a.scale_log2, a.seq, a.err);
   return note_cuda(cudaGetLastError(), "dK/dV kernel launch");
 }

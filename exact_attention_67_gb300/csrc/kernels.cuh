@@ -87,6 +87,9 @@ __host__ __device__ __forceinline__ GridPos grid_pos(int block, int BH, int n_ti
 // query tile's TMEM (dQ 64 + S 96 + dP 96 columns) still fits two tiles in
 // 512 columns and each step's fixed hand-off latencies cover more keys.
 constexpr int dq_key_step(int d) { return d == 64 ? 96 : 64; }
+// Queries per step of the dK/dV kernel, likewise: 64 at d = 128; 96 at d = 64
+// (dK, dV 64 columns each, two buffers of S^T and dP^T of 96 columns).
+constexpr int dkdv_query_step(int d) { return d == 64 ? 96 : 64; }
 
 // Problems per group for grid_pos: as many as keep their re-read operands
 // (bytes_per_problem each) within `budget` bytes of the 129 MB L2 (half of
@@ -145,6 +148,9 @@ struct BwdArgs {
   // K and V with a box of dq_key_step(d) rows: the dQ kernel's key tiles
   const CUtensorMap* tm_kdq;
   const CUtensorMap* tm_vdq;
+  // Q and dO with a box of dkdv_query_step(d) rows: the dK/dV kernel's query tiles
+  const CUtensorMap* tm_qkv;
+  const CUtensorMap* tm_dokv;
   const void* o;            // [B, H, N, d] views (d contiguous) with their element strides
   Strides so;
   const void* dO;
