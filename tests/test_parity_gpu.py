@@ -56,36 +56,33 @@ def test_wide_logits_rescale(orc):
     print(msg)
 
 
-@pytest.mark.parametrize("cfg", [3, 4, 5])
-def test_workload_sampled_parity(orc, cfg):
-    """Full-size workloads in the benchmark's launch configuration, checked on
+def sampled_parity(orc, name, B, H, N, causal, scale, ins, bwd, seed):
+    """Full-size problem in the benchmark's launch configuration, checked on
     sampled rows the oracle computes one by one (two heads, ~100 rows each),
     and key gradients on one head (needs that head's full row statistics)."""
-    w = WORKLOADS[cfg]
-    ins = make_inputs(w)
     q, k, v = ins[:3]
-    do = ins[3] if w.bwd else None
-    res = run_gpu(q, k, v, do, w.causal, w.scale, bwd=w.bwd)
-    BH = w.B * w.H
+    do = ins[3] if bwd else None
+    res = run_gpu(q, k, v, do, causal, scale, bwd=bwd)
+    BH = B * H
     heads = [0, BH - 1]
     msgs = []
     for hidx in heads:
-        b, h = divmod(hidx, w.H)
-        rows = sample_rows(w.N, 96, seed=cfg * 100 + hidx)
+        b, h = divmod(hidx, H)
+        rows = sample_rows(N, 96, seed=seed + hidx)
         qf, kf, vf = to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h])
-        o_ref, lse_ref = orc.head_fwd(qf, kf, vf, w.causal, w.scale, rows=rows)
+        o_ref, lse_ref = orc.head_fwd(qf, kf, vf, causal, scale, rows=rows)
         msgs.append(check_fwd(to_f64(res["o"][b, h])[rows], res["lse"][b, h].double().numpy()[rows], o_ref,
-                              lse_ref, f"{w.name} head {hidx}"))
-        if w.bwd:
-            krows = sample_rows(w.N, 48, seed=cfg * 100 + hidx + 7) if hidx == heads[0] else np.zeros(0, np.int32)
-            dq_ref, dk_ref, dv_ref = orc.head_bwd(qf, kf, vf, to_f64(do[b, h]), w.causal, w.scale, qrows=rows,
+                              lse_ref, f"{name} head {hidx}"))
+        if bwd:
+            krows = sample_rows(N, 48, seed=seed + hidx + 7) if hidx == heads[0] else np.zeros(0, np.int32)
+            dq_ref, dk_ref, dv_ref = orc.head_bwd(qf, kf, vf, to_f64(do[b, h]), causal, scale, qrows=rows,
                                                   krows=krows)
             pairs = [("dQ", to_f64(res["dq"][b, h])[rows], dq_ref)]
             if krows.size:
                 pairs += [("dK", to_f64(res["dk"][b, h])[krows], dk_ref),
                           ("dV", to_f64(res["dv"][b, h])[krows], dv_ref)]
-            msgs.append(check_grads(pairs, f"{w.name} head {hidx}"))
-    if w.bwd:
+            msgs.append(check_grads(pairs, f"{name} head {hidx}"))
+    if bwd:
         # Properties that hold at any size: sum_j dK_j = 0, sum_j dV_j = sum_i dO_i (per head).
         dk = res["dk"].double()
         dv = res["dv"].double()
@@ -94,6 +91,23 @@ def test_workload_sampled_parity(orc, cfg):
         assert (dk.sum(dim=2).abs().max().item()) <= 2e-2 * scale_k
         assert ((dv.sum(dim=2) - dsum).abs().max().item()) <= 2e-2 * dv.abs().sum(dim=2).max().item()
     print("\n".join(msgs))
+
+
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_workload_sampled_parity(orc, cfg):
+    w = WORKLOADS[cfg]
+    sampled_parity(orc, w.name, w.B, w.H, w.N, w.causal, w.scale, make_inputs(w), w.bwd, seed=cfg * 100)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d64_backward_at_full_size(orc, causal):
+    """The d = 64 backward (dQ in 96-key steps, dK/dV in 96-query steps with
+    three elementwise warpgroups, heads in L2-sized groups over many waves) at
+    the B4 H32 N4096 size of the d = 64 workload, whose own definition is
+    forward-only."""
+    w, ins = custom(4, 32, 4096, 64, causal, seed=4100 + int(causal))
+    sampled_parity(orc, f"B4 H32 N4096 d64 causal={causal}", 4, 32, 4096, causal, w.scale, ins, True,
+                   seed=700 + int(causal))
 
 
 @pytest.mark.parametrize("cfg", [3, 4, 5])
