@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
         ddc[u] = ndd[u];
       }
       fetch_terms(it + 1, nl2, ndd);
-      if (!mbar_wait(&bars->st_empty[s], ph ^ 1, wc)) break;
+      if (!mbar_wait_warp(&bars->st_empty[s], ph ^ 1, wc)) break;
       if (lane == 0) EXATTN_TRACE_POINT(0, it, 0);
       const int qi0 = (i_begin + it) * C::BR;
       float* st_lse2 = stat + s * 2 * C::BR;
@@ -387,6 +387,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
     bool ok = true;
     for (int it = 0; ok && it < nq; ++it) {
       const int s = it % C::STAGES, b = it & 1;
+      // Per-thread waits on the step's hand-offs (warp-uniform ones cost
+      // 1.3 % at d = 64): the lanes enter them converged and see the same
+      // barrier phase, abort flag and timer, so they leave them together.
       if (!(ok = mbar_wait(&bars->s_full[b], (it >> 1) & 1, wc))) break;
       if (threadIdx.x == 0) EXATTN_TRACE_POINT(2, it, 0);
       // The row statistics of this step were written by the producer's threads.
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::THREADS, 1)
       mbar_arrive(&bars->p_full[b]);
     }
     // The first four warps write dK and dV.
-    if (ok && group == 0) ok = mbar_wait(&bars->acc_done, 0, wc);
+    if (ok && group == 0) ok = mbar_wait_warp(&bars->acc_done, 0, wc);
     if (ok && group == 0) {
       tc_fence_after();
 

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                                o + bt * so.b + hh * so.h + static_cast<long long>(row0 + rr) * so.n) + part)
                          : make_uint4(0u, 0u, 0u, 0u);
         }
-        ok = mbar_wait(&bars->qd_full[t], 0, wc);
+        ok = mbar_wait_warp(&bars->qd_full[t], 0, wc);
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
           const int r = wq * 32 + i * RPW + sub;  // row within the tile
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         for (int i = 0; i < NI; ++i) finish(i, acc[i]);
       } else {
         // fp32 O, contiguous [B*H, N, d] rows (fixed-length calls only).
-        ok = mbar_wait(&bars->qd_full[t], 0, wc);
+        ok = mbar_wait_warp(&bars->qd_full[t], 0, wc);
 #pragma unroll 4
         for (int i = 0; i < NI; ++i) {
           const int r = wq * 32 + i * RPW + sub;
@@ -383,6 +383,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       Drow = Dws[sr0.stat0 + qrow];
     }
     for (int it = 0; ok && it < nk_t; ++it) {
+      // Per-thread wait on the step's hand-off (a warp-uniform one cost dQ
+      // 1.5 %): the lanes enter it converged and see the same barrier phase,
+      // abort flag and timer, so they leave it together.
       if (!(ok = mbar_wait(&bars->s_full[t], it & 1, wc))) break;
       if (row == 0) EXATTN_TRACE_POINT(2 + t, it, 0);
       tc_fence_after();
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
     }
-    if (ok && nk_t > 0) ok = mbar_wait(&bars->acc_done[t], 0, wc);
+    if (ok && nk_t > 0) ok = mbar_wait_warp(&bars->acc_done[t], 0, wc);
     if (ok && nk_t > 0) {
       tc_fence_after();
       T* dst_row = dq + bt * sdq.b + hh * sdq.h + static_cast<long long>(row0 + qrow) * sdq.n;

@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(FwdThreads<T>::value, 1)
     }
     // ---------------------------------------------------------- epilogue
     const bool any = (t == 0 ? nkv0 : nkv1) > 0;
-    if (ok && any) ok = mbar_wait(&bars->o_full[t], 0, wc);
+    if (ok && any) ok = mbar_wait_warp(&bars->o_full[t], 0, wc);
     if (ok && kv.part_o) {
       // Key split: this split's O (normalised within it) and both
       // logsumexps in fp32; a row that saw no key here gets O = 0 and -inf.

@@ -134,7 +134,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 
 // The same wait made by a whole converged warp, which gives up as one: code
 // that ends with a per-warp arrive (mbar_arrive_warp) must not leave a lane
-// behind in the loop.
+// behind in the loop, and the warp-collective TMEM loads and stores
+// (.sync.aligned) after a wait need every lane on the same side of it.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
