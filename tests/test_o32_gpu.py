@@ -102,3 +102,23 @@ def test_autograd_fp32_o_matches_the_o32_calls():
     torch.cuda.synchronize()
     assert torch.equal(out.detach(), o)
     assert torch.equal(qa.grad, dq) and torch.equal(ka.grad, dk) and torch.equal(va.grad, dv)
+
+
+@pytest.mark.parametrize("d,causal,window", [(64, True, 100), (128, False, 57)])
+def test_autograd_fp32_o_with_window_against_the_oracle(orc, d, causal, window):
+    """attention(..., fp32_o=True) with a sliding window, f16 inputs in the
+    [B, N, H, d] layout: gradients match the fp64 oracle, and the output
+    equals the default path's (the fp32 copy changes only the row terms)."""
+    import exact_attention_67_gb300 as ex
+    w, ins = custom(1, 3, 410, d, causal, seed=71 + d, dtype=torch.float16)
+    q, k, v, do = (t.to(DEV) for t in ins)
+    qn, kn, vn = (t.transpose(1, 2).contiguous().transpose(1, 2).requires_grad_(True) for t in (q, k, v))
+    out = ex.attention(qn, kn, vn, causal=causal, scale=w.scale, window=window, fp32_o=True)
+    out.backward(do)
+    o_default = ex.attention(q, k, v, causal=causal, scale=w.scale, window=window)
+    torch.cuda.synchronize()
+    assert torch.equal(out.detach(), o_default)
+    qf, kf, vf, dof = (to_f64(t) for t in ins)
+    dq_ref, dk_ref, dv_ref = orc.attention_bwd(qf, kf, vf, dof, causal, w.scale, window=window)
+    print(check_grads([("dQ", to_f64(qn.grad.cpu()), dq_ref), ("dK", to_f64(kn.grad.cpu()), dk_ref),
+                       ("dV", to_f64(vn.grad.cpu()), dv_ref)], f"fp32_o autograd d{d} window {window}"))
