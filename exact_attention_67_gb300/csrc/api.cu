@@ -96,34 +96,40 @@ int device_setup(int* dev_out, unsigned** err_out) {
     note_failure("cudaGetDevice (device ordinal out of range)", static_cast<int>(cudaErrorInvalidDevice), false);
     return EXATTN_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState& st = g_dev[dev];
-  if (!st.ready) {
-    int major = 0, minor = 0;
-    if (note_cuda(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute") !=
-            cudaSuccess ||
-        note_cuda(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute") !=
-            cudaSuccess) {
-      return EXATTN_ERR_CUDA;
-    }
-    if (major != 10 || minor != 3) {
-      st.status = EXATTN_ERR_ARCH;
-    } else {
-      void* p = nullptr;
-      if (note_cuda(cudaGetSymbolAddress(&p, g_err_word), "cudaGetSymbolAddress") != cudaSuccess)
+  int status;
+  unsigned* err;
+  {
+    // Set-up under the lock; afterwards the state is only read.
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+      int major = 0, minor = 0;
+      const char* what = "cudaDeviceGetAttribute";
+      if (note_cuda(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), what) != cudaSuccess ||
+          note_cuda(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), what) != cudaSuccess)
         return EXATTN_ERR_CUDA;
-      st.err = static_cast<unsigned*>(p);
-      if (!g_encode || !g_ctx_current) {
-        void *enc = nullptr, *cur = nullptr;
-        if (!driver_fn("cuTensorMapEncodeTiled", &enc) || !driver_fn("cuCtxGetCurrent", &cur)) return EXATTN_ERR_CUDA;
-        g_encode = reinterpret_cast<EncodeTiledFn>(enc);
-        g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(cur);
+      if (major != 10 || minor != 3) {
+        st.status = EXATTN_ERR_ARCH;
+      } else {
+        void* p = nullptr;
+        if (note_cuda(cudaGetSymbolAddress(&p, g_err_word), "cudaGetSymbolAddress") != cudaSuccess)
+          return EXATTN_ERR_CUDA;
+        st.err = static_cast<unsigned*>(p);
+        if (!g_encode || !g_ctx_current) {
+          void *enc = nullptr, *cur = nullptr;
+          if (!driver_fn("cuTensorMapEncodeTiled", &enc) || !driver_fn("cuCtxGetCurrent", &cur))
+            return EXATTN_ERR_CUDA;
+          g_encode = reinterpret_cast<EncodeTiledFn>(enc);
+          g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(cur);
+        }
+        st.status = EXATTN_OK;
       }
-      st.status = EXATTN_OK;
+      st.ready = true;
     }
-    st.ready = true;
+    status = st.status;
+    err = st.err;
   }
-  if (st.status != EXATTN_OK) return st.status;
+  if (status != EXATTN_OK) return status;
   CUcontext ctx = nullptr;
   const CUresult r = g_ctx_current(&ctx);
   if (r != CUDA_SUCCESS) {
@@ -132,7 +138,7 @@ int device_setup(int* dev_out, unsigned** err_out) {
   }
   if (!ctx && note_cuda(cudaSetDevice(dev), "cudaSetDevice") != cudaSuccess) return EXATTN_ERR_CUDA;
   *dev_out = dev;
-  *err_out = st.err;
+  *err_out = err;
   return EXATTN_OK;
 }
 
