@@ -631,13 +631,28 @@ struct DecodePlan {
 
 DecodePlan decode_plan(int B, int H, int Nq, int Nk, int d) {
   const long long nkt = (Nk + 127) / 128;
-  const int n_pairs = (Nq + 255) / 256;
-  const long long base = static_cast<long long>(n_pairs) * B * H;
-  long long splits = std::min(nkt, std::max(1ll, (304 + base - 1) / base));
-  splits = std::min(splits, std::max(1ll, nkt / 2));
+  long long splits;
+  int nq_pad;
+  if (Nq <= kDecodeMaxQ && d == 128) {
+    // The decode kernel: one CTA per (batch, head) and key split, about two
+    // CTAs per SM, and at least four key tiles per split where the keys
+    // allow it (a CTA's set-up and epilogue cost about as much as a few
+    // tiles' loads).
+    const long long bh = static_cast<long long>(B) * H;
+    splits = std::min(nkt, std::max(1ll, (304 + bh - 1) / bh));
+    splits = std::min(splits, std::max(1ll, nkt / 4));
+    nq_pad = kDecodeQCols;
+  } else {
+    // The forward kernel with its keys split: pairs of 128-row query tiles.
+    const int n_pairs = (Nq + 255) / 256;
+    const long long base = static_cast<long long>(n_pairs) * B * H;
+    splits = std::min(nkt, std::max(1ll, (304 + base - 1) / base));
+    splits = std::min(splits, std::max(1ll, nkt / 2));
+    nq_pad = n_pairs * 256;
+  }
   const long long tps = (nkt + splits - 1) / splits;
   splits = (nkt + tps - 1) / tps;
-  DecodePlan p{static_cast<int>(splits), static_cast<int>(tps), n_pairs * 256, 0, 0, 0};
+  DecodePlan p{static_cast<int>(splits), static_cast<int>(tps), nq_pad, 0, 0, 0};
   if (p.n_splits > 1) {
     const size_t rows = static_cast<size_t>(p.n_splits) * B * H * p.nq_pad;
     p.o_bytes = (rows * d * sizeof(float) + 255) & ~size_t(255);
@@ -684,8 +699,10 @@ extern "C" int attn_fwd_decode(int dtype, const void* q, exattn_strides sq, cons
   unsigned* err = nullptr;
   if ((rc = device_setup(&dev, &err)) != EXATTN_OK) return rc;
   const int dt = dtype == EXATTN_DTYPE_F16 ? kF16 : kBF16;
+  const bool few_queries = Nq <= kDecodeMaxQ && d == 128;  // the decode kernel, else the forward with key splits
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, dt, B, H, Nq, d, to_strides(sq), 128) || !make_map(&mk, k, dt, B, H, Nk, d, to_strides(sk), 128) ||
+  if (!make_map(&mq, q, dt, B, H, Nq, d, to_strides(sq), few_queries ? kDecodeQCols : 128) ||
+      !make_map(&mk, k, dt, B, H, Nk, d, to_strides(sk), 128) ||
       !make_map(&mv, v, dt, B, H, Nk, d, to_strides(sv), 128))
     return EXATTN_ERR_CUDA;
   FwdArgs a{};
@@ -717,7 +734,7 @@ extern "C" int attn_fwd_decode(int dtype, const void* q, exattn_strides sq, cons
   a.err = err;
   a.device = dev;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_fwd(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if ((few_queries ? launch_decode(a, st) : launch_fwd(a, st)) != cudaSuccess) return EXATTN_ERR_CUDA;
   if (plan.n_splits > 1 && launch_fwd_merge(a, st) != cudaSuccess) return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
