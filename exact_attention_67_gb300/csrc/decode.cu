@@ -1,5 +1,5 @@
 // decode.cu -- the decode-shaped forward for a few queries against many keys
-// (at d = 128, Nq <= 8 query rows per (batch, head), queries at the last Nq
+// (at d = 128, Nq <= 12 query rows per (batch, head), queries at the last Nq
 // key positions), for sm_103a.
 //
 // The forward kernel runs a 128-row query tile per MMA; with one to sixteen
@@ -10,7 +10,10 @@
 // operands exchanged):
 //   * S^T = K_j Q^T: M = 128 keys (TMEM lanes), N = 16 query columns, K = d;
 //   * the online softmax runs down each query column: every thread holds one
-//     key's 16 scores, the column maxima are reduced across the warpgroup;
+//     key's 16 scores; a column's reference max moves only when a score
+//     beats it by 2^8 (or the column sees its first key), so a step first
+//     trades one bit per column between the four warps, and only a step
+//     that needs it reduces the column maxima across the warpgroup;
 //   * O^T += V_j^T P^T: M = d = 128 rows (TMEM lanes), N = 16, K = 128 keys,
 //     with P^T written by the elementwise threads into shared memory in f16;
 //   * the epilogue reads O^T row d of every query column from lane d, so the
@@ -18,11 +21,11 @@
 // Keys are split over CTAs (as in the forward's key split) and the splits'
 // fp32 partial O and logsumexps are combined by the forward's merge kernel.
 // Measured against the forward kernel's key-split path on the same GPU (B8
-// H16 Nk16384 and B4 H32 Nk32768, d = 128): 1.26x faster for Nq <= 4, 1.1x
-// for 6-8, slower from 12 queries on (the per-key column work grows with Nq
-// while the forward's softmax runs along rows), and at d = 64 slower for
-// every Nq (a step moves half the bytes for the same column work), hence
-// the d = 128, Nq <= 8 dispatch in the C ABI.
+// H16 Nk16384 and B4 H32 Nk32768, d = 128): 1.26x faster for Nq <= 4,
+// 1.17x at 8, 1.07-1.10x at 12, slower at 16 (the per-key column work
+// grows with Nq while the forward's softmax runs along rows); at d = 64 a
+// step moves half the bytes for the same column work and the kernel was
+// slower for every Nq.  Hence the d = 128, Nq <= 12 dispatch in the C ABI.
 //
 // CTA: warps 0-3 elementwise (thread = key row of S^T and row d of O^T),
 // warp 4 TMA producer, warp 5 MMA issuer, and for bf16 inputs warps 6-7
@@ -59,8 +62,10 @@ struct DecCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
   static constexpr int OFF_Q = OFF_V + STAGES * KV_TILE;
   static constexpr int OFF_P = OFF_Q + Q_TILE;             // two P^T buffers
-  static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // column maxima [2][4 warps][16], sums [4][16]
-  static constexpr int OFF_BAR = OFF_RED + 3 * 4 * NQ * 4;
+  // Column maxima [2][4 warps][16] and sums [4][16] (floats), then the
+  // warps' need-a-new-max bits [2][4] (32-bit words).
+  static constexpr int OFF_RED = OFF_P + 2 * P_TILE;
+  static constexpr int OFF_BAR = OFF_RED + 3 * 4 * NQ * 4 + 2 * 4 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit");
   static constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
@@ -303,6 +308,7 @@ __global__ void __launch_bounds__(DecThreads<T>::value, 1)
       const int b = j & 1;
       float x[NQ];
       float* rb = red + b * 4 * NQ;  // the four warps' column maxima, buffer j % 2
+      uint32_t need = 0;             // bit q: column q's reference max must move
       if (ok) ok = mbar_wait_warp(&bars->s_full[b], (j >> 1) & 1, wc);
       if (ok) {
         tc_fence_after();
@@ -313,50 +319,82 @@ __global__ void __launch_bounds__(DecThreads<T>::value, 1)
         tc_fence_before();
         mbar_arrive_warp(&bars->s_free[b]);  // the MMA warp may compute S^T_{j+2} into buffer b
         // Scaled logits of this thread's key for each query column; hidden
-        // ones (and columns past Nq) -inf.  Columns go in groups of four up
-        // to Nq: within a group the four butterflies interleave.
-        const int kj = (t_lo + j) * BN + tid;
+        // ones (and columns past Nq, within the last group of four) -inf.
+        // Per-element masks only on tiles where some query cannot see some
+        // key: past Nk, past the diagonal, or outside a window.
+        const int kj0 = (t_lo + j) * BN, kj = kj0 + tid;
+        const bool need_mask = kj0 + BN > Nk || (CAUSAL && kj0 + BN - 1 > off) ||
+                               (window > 0 && (off + Nq - 1 - kj0 >= window ||
+                                               (!CAUSAL && kj0 + BN - 1 - off >= window)));
 #pragma unroll
-        for (int g = 0; g < NQ / 4; ++g) {
-          if (4 * g >= Nq) break;
-          float v[4];
+        for (int q = 0; q < NQ; ++q) {
+          if (4 * (q >> 2) >= Nq) break;  // whole groups of four columns up to Nq
+          const int pos = off + q;
+          bool vis = q < Nq;
+          if (need_mask)
+            vis = vis && kj < Nk && (!CAUSAL || kj <= pos) &&
+                  (window == 0 || (pos - kj < window && (CAUSAL || kj - pos < window)));
+          x[q] = vis ? __uint_as_float(sv[q]) * scale_log2 : -INFINITY;
+          // The column's reference max must move: a score beats it by the
+          // threshold, or the column sees its first key.
+          if (x[q] > m_ref[q] + kDecRescale || (m_ref[q] == -INFINITY && x[q] != -INFINITY)) need |= 1u << q;
+        }
+        need = __reduce_or_sync(0xffffffffu, need);
+      }
+      // The warps trade their need bits (buffer j % 2, written again two
+      // steps on, after every warp has passed the next step's barrier, by
+      // which time all have read it).
+      uint32_t* flags = reinterpret_cast<uint32_t*>(red + 3 * 4 * NQ) + b * 4;
+      if (lane == 0) flags[warp] = need;
+      named_bar_sync(1, 128);
+      const uint32_t need_all = flags[0] | flags[1] | flags[2] | flags[3];
+      float alpha[NQ];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = 4 * g + u, pos = off + q;
-            const bool vis = q < Nq && kj < Nk && (!CAUSAL || kj <= pos) &&
-                             (window == 0 || (pos - kj < window && (CAUSAL || kj - pos < window)));
-            x[q] = vis ? __uint_as_float(sv[q]) * scale_log2 : -INFINITY;
-            v[u] = x[q];
+      for (int q = 0; q < NQ; ++q) alpha[q] = 1.f;
+      bool rescale = false;  // the same in every thread: all read the same maxima
+      if (need_all != 0) {
+        // Some column's reference max moves (the first steps, and rarely
+        // after): the column maxima over the step's 128 keys, butterflies per
+        // warp in groups of four that interleave, then the four warps through
+        // shared memory.  Every warp takes this branch (the bits are common),
+        // so the second barrier is met by all of them too.
+        if (ok) {
+#pragma unroll
+          for (int g = 0; g < NQ / 4; ++g) {
+            if (4 * g >= Nq) break;
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = x[4 * g + u];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) v[u] = fmaxf(v[u], __shfl_xor_sync(0xffffffffu, v[u], o));
+            if (lane == 0) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) rb[warp * NQ + 4 * g + u] = v[u];
+            }
           }
+        }
+        named_bar_sync(1, 128);
+        if (ok) {
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = fmaxf(v[u], __shfl_xor_sync(0xffffffffu, v[u], o));
-          if (lane == 0) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) rb[warp * NQ + 4 * g + u] = v[u];
+          for (int q = 0; q < NQ; ++q) {
+            if (4 * (q >> 2) >= Nq) break;
+            if (!((need_all >> q) & 1u)) continue;
+            const float mstep = fmaxf(fmaxf(rb[q], rb[NQ + q]), fmaxf(rb[2 * NQ + q], rb[3 * NQ + q]));
+            if (m_ref[q] != -INFINITY) {
+              alpha[q] = ex2(m_ref[q] - mstep);
+              rescale = true;
+            }
+            m_ref[q] = mstep;
           }
         }
       }
-      // Buffer b is written again two steps on, after every warp has passed
-      // the next step's barrier, by which time all have read it.
-      named_bar_sync(1, 128);
       if (!ok) continue;
-      float alpha[NQ];
-      bool rescale = false;  // the same in every thread: all read the same maxima
       __half ph[NQ];
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
-        if (4 * (q >> 2) >= Nq) break;  // whole groups of four, as above
-        const float mstep = fmaxf(fmaxf(rb[q], rb[NQ + q]), fmaxf(rb[2 * NQ + q], rb[3 * NQ + q]));
-        alpha[q] = 1.f;
-        if (m_ref[q] == -INFINITY) {
-          m_ref[q] = mstep;  // first visible scores of the column (or still none)
-        } else if (mstep > m_ref[q] + kDecRescale) {
-          alpha[q] = ex2(m_ref[q] - mstep);
-          m_ref[q] = mstep;
-          rescale = true;
-        }
+        if (4 * (q >> 2) >= Nq) break;
         // Weights rounded to f16 as the P V product takes them; the row sums
         // are formed from the rounded values.
         const float p = m_ref[q] == -INFINITY ? 0.f : ex2(x[q] - m_ref[q]);

@@ -191,8 +191,8 @@ cudaError_t launch_fwd_merge(const FwdArgs& a, cudaStream_t stream);
 // (decode.cu): a.tm_q with a box of kDecodeQCols rows, a.kv as for the
 // forward's key split (nq_pad = kDecodeQCols, n_splits >= 1; partials in
 // a.kv.part_o when n_splits > 1).  Measured faster than the forward kernel
-// with split keys up to 8 queries at d = 128, slower beyond and at d = 64.
-constexpr int kDecodeMaxQ = 8;
+// with split keys up to 12 queries at d = 128, slower at 16.
+constexpr int kDecodeMaxQ = 12;
 constexpr int kDecodeQCols = 16;  // query columns of the kernel (the MMA's N)
 cudaError_t launch_decode(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);

@@ -1,6 +1,6 @@
 """GPU parity of the decode-shaped forward (attn_fwd_decode): Nq queries
 against Nk keys, the queries being the last Nq positions of the sequence
-(at d = 128 with at most 8 queries through the decode kernel, otherwise
+(at d = 128 with at most 12 queries through the decode kernel, otherwise
 through the forward kernel with split keys).
 Reference: the fp64 oracle on the square problem whose last Nq query rows
 are these queries (the oracle's rows= selection), so the alignment, the
@@ -35,11 +35,13 @@ CASES = [
     (1, 2, 16, 9000, 64, True, 300, torch.bfloat16),
     (1, 1, 1, 1, 128, True, 0, torch.bfloat16),
     (2, 2, 300, 300, 128, True, 0, torch.float16),
-    # d = 128 and at most 8 queries: the decode kernel (keys on the MMA's M side)
+    # d = 128 and at most 12 queries: the decode kernel (keys on the MMA's M side)
     (2, 3, 5, 6000, 128, False, 700, torch.float16),
     (1, 2, 8, 50000, 128, True, 0, torch.bfloat16),
     (3, 110, 2, 1100, 128, True, 0, torch.bfloat16),
     (1, 1, 3, 129, 128, True, 64, torch.bfloat16),
+    (2, 2, 12, 7000, 128, True, 0, torch.float16),
+    (1, 3, 11, 2500, 128, False, 900, torch.bfloat16),
 ]
 
 
