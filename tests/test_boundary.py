@@ -277,6 +277,29 @@ def test_decode_validation(lib):
     assert dec(B=1, H=1, Nq=1, Nk=32768, ws=P[5], wsb=ws - 1) == 6
 
 
+def test_decode_plan_sizes(lib):
+    """The decode call's workspace follows its plan: at d = 128 with at most
+    12 queries the decode kernel (16 query columns per split row), otherwise
+    the forward kernel with split keys (256-row query pairs); about 2 x 152
+    CTAs, at least four key tiles per split for the decode kernel and two
+    for the forward's.  Sizes: split partials fp32 [splits, B*H, rows, d]
+    plus two fp32 logsumexps [splits, B*H, rows], each 256-byte aligned."""
+    def size(splits, bh, rows, d):
+        n = splits * bh * rows
+        up = lambda x: (x + 255) // 256 * 256
+        return up(n * d * 4) + 2 * up(n * 4)
+    # B4 H32 Nk32768 d128: 256 key tiles, 3 splits of 86 tiles.
+    assert lib.attn_fwd_decode_workspace_size(4, 32, 1, 32768, 128) == size(3, 128, 16, 128)
+    assert lib.attn_fwd_decode_workspace_size(4, 32, 12, 32768, 128) == size(3, 128, 16, 128)
+    assert lib.attn_fwd_decode_workspace_size(4, 32, 13, 32768, 128) == size(3, 128, 256, 128)
+    # d = 64 always takes the forward kernel.
+    assert lib.attn_fwd_decode_workspace_size(8, 16, 1, 16384, 64) == size(3, 128, 256, 64)
+    # One head, 1024 key tiles: 256 splits of four tiles (the decode kernel's floor).
+    assert lib.attn_fwd_decode_workspace_size(1, 1, 1, 131072, 128) == size(256, 1, 16, 128)
+    # The forward kernel's plan for 16 queries: 304 splits wanted, 4 tiles each, hence 256.
+    assert lib.attn_fwd_decode_workspace_size(1, 1, 16, 131072, 128) == size(256, 1, 256, 128)
+
+
 def test_host_path_rejects_bad_tensors():
     """fwd_bwd_from_host checks its host tensors before any device work."""
     import torch
