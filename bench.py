@@ -92,12 +92,40 @@ def load_peaks():
                 "source": "fallback"}
 
 
+def code_tokens(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of white
+    space made one blank: what the compiler sees, so that editing a comment
+    does not mark a profiled kernel as changed.  String and character
+    literals are kept as written."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif c == "/" and text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha(name: str) -> str:
     src = {"attn_fwd_kernel": "fwd.cu", "bwd_dkdv_kernel": "bwd.cu", "bwd_dq_kernel": "dq.cu"}[name]
     h = hashlib.sha256()
     for f in (src, "ptx.cuh", "kernels.cuh"):
-        with open(os.path.join(ROOT, "exact_attention_67_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "exact_attention_67_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -21,8 +21,10 @@
 //      S^T/dP^T are double buffered so the next tile's products overlap the
 //      current elementwise work.
 //   3. bwd_dq_kernel (dq.cu): two 128-query tiles per CTA; streams key
-//      tiles of K and V; S = Q K_j^T and dP = dO V_j^T into TMEM, dS (input
-//      type) written back, and dQ += dS K_j accumulated in TMEM.
+//      tiles (64 keys at d = 128, 96 at d = 64) of K and V; S = Q K_j^T and
+//      dP = dO V_j^T into TMEM, dS (input type) written back, and
+//      dQ += dS K_j accumulated in TMEM.  In attn_bwd it runs first and
+//      also forms D_i for its rows, which bwd_dkdv_kernel then reads.
 // Causal: key tiles wholly above the diagonal are skipped, diagonal tiles are
 // masked element by element (key j visible to query i iff j <= i).
 #include "kernels.cuh"

@@ -93,3 +93,29 @@ def test_bench_gpus_2_without_gpus_fails_loudly():
     r = _bench("--gpus", "2", "--steps", "1", "--warmup", "3", "--no-cpu-baseline", "--no-e2e", "--no-clocks")
     assert r.returncode != 0
     assert "needs CUDA device" in (r.stdout + r.stderr)
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_for_hash", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_kernel_hash_ignores_comments_and_layout_but_not_code():
+    """The DRAM-traffic entries of the bench line are tied to the code of the
+    kernel they were captured on: editing a comment or re-indenting keeps
+    them, any change of a token drops them."""
+    b = _bench_module()
+    src = ('// head\nint f(int x) {  /* block\n comment */ return x + 1;  // tail\n}\n'
+           'const char* s = "a // not a comment /* nor this */";\nchar c = \'/\';\n')
+    same = ('int f(int x)\n{\n    return x + 1;\n}  // another note\n'
+            'const char* s = "a // not a comment /* nor this */";  /* x */ char c = \'/\';')
+    assert b.code_tokens(src) == b.code_tokens(same)
+    assert '"a // not a comment /* nor this */"' in b.code_tokens(src)
+    for changed in (src.replace("x + 1", "x + 2"), src.replace("not a comment", "not a comment!"),
+                    src.replace("'/'", "'*'")):
+        assert b.code_tokens(changed) != b.code_tokens(src)
+    # The escape inside a literal does not end it early.
+    assert b.code_tokens('s = "q\\" // kept"; // dropped') == 's = "q\\" // kept";'
