@@ -20,7 +20,12 @@
 //     tile 0 / tile 1 (thread = query row); while one warpgroup works, the
 //     tensor core runs the other tile's MMAs, which hides the hand-off
 //     latency between the two roles;
-//   * warp 8 issues the TMA loads.
+//   * warp 8 issues the TMA loads;
+//   * when the kernel forms the row terms (attn_bwd), warps 0-7 first compute
+//     D_i = dO_i . O_i for their rows, O read from global memory and dO from
+//     its tile in shared memory, with the separate row-dot kernel's lane
+//     grouping and summation order (bit-identical D), and store D for the
+//     dK/dV kernel that runs next.
 // TMEM per tile t (base 256 t): d = 128: dQ_t [0,128), S_t [128,192), dP_t
 // [192,256); d = 64: dQ_t [0,64), S_t [64,160), dP_t [160,256).
 // Causal: key tiles above the diagonal are skipped per query tile, diagonal

@@ -21,8 +21,9 @@
 //     128 scores, updates the running max, rescales the running sum and the
 //     TMEM O row when the max has grown by more than 2^8 (the reference max
 //     is otherwise kept; the final normalisation by the same reference makes
-//     the result identical), writes P = 2^(s*scale*log2e - m) as f16 over
-//     the S columns, and hands the tile back to the MMA warp.  While one
+//     the result identical), writes P = 2^(s*scale*log2e - m) as f16 into
+//     TMEM (over the S columns at d = 128, in columns of its own at d = 64),
+//     and hands the tile back to the MMA warp.  While one
 //     warpgroup does its softmax the tensor core works on the other tile.
 //   * P V runs in f16 whatever the input type: P rounded to f16 (11
 //     significant bits) errs 8x less than bf16 (8 bits), which keeps O within
@@ -31,7 +32,8 @@
 //     tile to f16 in shared memory, in place, between its TMA landing and its
 //     first P V (exact for 2^-14 <= |v| <= 65504 and for 0; smaller
 //     magnitudes are carried with an absolute error below 2^-25).
-//   * epilogue: O_t / l rounded to the input type, lse = (m + log2 l) ln 2,
+//   * epilogue: O_t / l rounded to the input type (and, when asked for, an
+//     fp32 copy of the same quotient), lse = (m + log2 l) ln 2,
 //     with l the sum of the f16-rounded P that the PV MMA used (one row sum:
 //     each normal f16 weight is within 2^-11 of its value, relative, so lse
 //     moves by at most 4.9e-4 against the sum of unrounded terms, plus
