@@ -622,32 +622,53 @@ extern "C" int attn_bwd_varlen(int dtype, const void* q, exattn_strides sq, cons
 
 namespace {
 
-// Key splits of a decode-shaped forward: enough CTAs for about two waves on
-// the 152 SMs, at least two 128-key tiles per split, no empty split.
+// Key splits of a decode-shaped forward (pick_splits below), no empty split.
 struct DecodePlan {
   int n_splits, tiles_per_split, nq_pad;
   size_t o_bytes, lse_bytes, total_bytes;
 };
 
+// Key splits for a grid of `units` CTAs per split level (one per (batch,
+// head), or per query-tile pair and (batch, head)) over nkt key tiles: the
+// count whose grid finishes first when every CTA costs its key tiles plus
+// a fixed set-up and epilogue of about three tiles' worth and the CTAs run
+// in waves of one per SM (both kernels hold most of an SM's shared memory).
+// A last wave that is nearly empty costs a whole CTA time, so a count that
+// fills one wave with longer CTAs beats one that spills a few CTAs into a
+// second.  At most about two waves of CTAs: beyond that every SM already
+// streams keys and more splits add only set-up costs.  At most max_splits
+// splits; ties go to fewer splits (less workspace, a smaller merge).
+long long pick_splits(long long units, long long nkt, long long max_splits) {
+  constexpr long long kSMs = 152, kFixedTiles = 3;
+  max_splits = std::min(max_splits, 2 * kSMs / std::max(1ll, units));
+  max_splits = std::max(1ll, std::min({max_splits, nkt, static_cast<long long>(kMaxSplits)}));
+  long long best = 1, best_cost = -1;
+  for (long long s = 1; s <= max_splits; ++s) {
+    const long long tps = (nkt + s - 1) / s, used = (nkt + tps - 1) / tps;
+    const long long cost = ((units * used + kSMs - 1) / kSMs) * (kFixedTiles + tps);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = used;
+    }
+  }
+  return best;
+}
+
 DecodePlan decode_plan(int B, int H, int Nq, int Nk, int d) {
   const long long nkt = (Nk + 127) / 128;
+  const long long bh = static_cast<long long>(B) * H;
   long long splits;
   int nq_pad;
   if (Nq <= kDecodeMaxQ && d == 128) {
-    // The decode kernel: one CTA per (batch, head) and key split, about two
-    // CTAs per SM, and at least four key tiles per split where the keys
-    // allow it (a CTA's set-up and epilogue cost about as much as a few
-    // tiles' loads).
-    const long long bh = static_cast<long long>(B) * H;
-    splits = std::min(nkt, std::max(1ll, (304 + bh - 1) / bh));
-    splits = std::min(splits, std::max(1ll, nkt / 4));
+    // The decode kernel: one CTA per (batch, head) and key split, at least
+    // four key tiles per split where the keys allow it.
+    splits = pick_splits(bh, nkt, nkt / 4);
     nq_pad = kDecodeQCols;
   } else {
-    // The forward kernel with its keys split: pairs of 128-row query tiles.
+    // The forward kernel with its keys split: pairs of 128-row query tiles,
+    // at least two key tiles per split.
     const int n_pairs = (Nq + 255) / 256;
-    const long long base = static_cast<long long>(n_pairs) * B * H;
-    splits = std::min(nkt, std::max(1ll, (304 + base - 1) / base));
-    splits = std::min(splits, std::max(1ll, nkt / 2));
+    splits = pick_splits(static_cast<long long>(n_pairs) * bh, nkt, nkt / 2);
     nq_pad = n_pairs * 256;
   }
   const long long tps = (nkt + splits - 1) / splits;

@@ -109,6 +109,8 @@ inline int l2_group(long long bytes_per_problem, int BH, long long budget = kL2G
 //   part_o    [n_splits, B*H, nq_pad, d]  O of the split (normalised within it)
 //   part_lse  [n_splits, B*H, nq_pad]     logsumexp of the split (for lse)
 //   part_lseb [n_splits, B*H, nq_pad]     logsumexp of the rounded weights (for O)
+constexpr int kMaxSplits = 512;  // key splits launch_fwd_merge combines at most
+
 struct KvSplit {
   int nk;  // 0: as many keys as queries, no offset
   int n_splits, tiles_per_split, nq_pad;

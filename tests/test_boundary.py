@@ -280,24 +280,36 @@ def test_decode_validation(lib):
 def test_decode_plan_sizes(lib):
     """The decode call's workspace follows its plan: at d = 128 with at most
     12 queries the decode kernel (16 query columns per split row), otherwise
-    the forward kernel with split keys (256-row query pairs); about 2 x 152
-    CTAs, at least four key tiles per split for the decode kernel and two
-    for the forward's.  Sizes: split partials fp32 [splits, B*H, rows, d]
-    plus two fp32 logsumexps [splits, B*H, rows], each 256-byte aligned."""
+    the forward kernel with split keys (256-row query pairs).  The split
+    count is the one whose grid ends first when a CTA costs its key tiles
+    plus three, CTAs run in waves of 152 (one per SM), at most about two
+    waves of CTAs, at least four key tiles per split for the decode kernel
+    and two for the forward's.  Sizes: split partials fp32
+    [splits, B*H, rows, d] plus two fp32 logsumexps [splits, B*H, rows], each
+    256-byte aligned; no workspace without a split."""
     def size(splits, bh, rows, d):
         n = splits * bh * rows
         up = lambda x: (x + 255) // 256 * 256
         return up(n * d * 4) + 2 * up(n * 4)
-    # B4 H32 Nk32768 d128: 256 key tiles, 3 splits of 86 tiles.
-    assert lib.attn_fwd_decode_workspace_size(4, 32, 1, 32768, 128) == size(3, 128, 16, 128)
-    assert lib.attn_fwd_decode_workspace_size(4, 32, 12, 32768, 128) == size(3, 128, 16, 128)
-    assert lib.attn_fwd_decode_workspace_size(4, 32, 13, 32768, 128) == size(3, 128, 256, 128)
-    # d = 64 always takes the forward kernel.
-    assert lib.attn_fwd_decode_workspace_size(8, 16, 1, 16384, 64) == size(3, 128, 256, 64)
-    # One head, 1024 key tiles: 256 splits of four tiles (the decode kernel's floor).
-    assert lib.attn_fwd_decode_workspace_size(1, 1, 1, 131072, 128) == size(256, 1, 16, 128)
-    # The forward kernel's plan for 16 queries: 304 splits wanted, 4 tiles each, hence 256.
-    assert lib.attn_fwd_decode_workspace_size(1, 1, 16, 131072, 128) == size(256, 1, 256, 128)
+    # B4 H32 Nk32768 d128: 128 heads fill one wave unsplit (3 + 256 = 259);
+    # two splits would take two waves of 3 + 128 (262).
+    assert lib.attn_fwd_decode_workspace_size(4, 32, 1, 32768, 128) == 0
+    assert lib.attn_fwd_decode_workspace_size(4, 32, 12, 32768, 128) == 0
+    assert lib.attn_fwd_decode_workspace_size(4, 32, 13, 32768, 128) == 0
+    # d = 64 takes the forward kernel; 128 heads, 128 key tiles: unsplit.
+    assert lib.attn_fwd_decode_workspace_size(8, 16, 1, 16384, 64) == 0
+    # One head, 1024 key tiles: 147 splits of 7 tiles fill one wave (cost
+    # 10); 8 tiles cost 11, and 4-6 tiles need a second wave (14 or more).
+    assert lib.attn_fwd_decode_workspace_size(1, 1, 1, 131072, 128) == size(147, 1, 16, 128)
+    assert lib.attn_fwd_decode_workspace_size(1, 1, 16, 131072, 128) == size(147, 1, 256, 128)
+    # 16 heads, 256 tiles: 9 splits of 29 tiles are 144 CTAs in one wave
+    # (32); 10 splits make 160 CTAs, two waves (58); 19 make two full
+    # waves (34).
+    assert lib.attn_fwd_decode_workspace_size(2, 8, 1, 32768, 128) == size(9, 16, 16, 128)
+    # 8 heads, 512 tiles: 19 splits of 27 tiles, exactly 152 CTAs.
+    assert lib.attn_fwd_decode_workspace_size(1, 8, 1, 65536, 128) == size(19, 8, 16, 128)
+    # 8 tiles: two splits of four (3 + 4) beat one CTA of eight (3 + 8).
+    assert lib.attn_fwd_decode_workspace_size(1, 1, 1, 1000, 128) == size(2, 1, 16, 128)
 
 
 def test_host_path_rejects_bad_tensors():

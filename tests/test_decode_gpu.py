@@ -42,6 +42,12 @@ CASES = [
     (1, 1, 3, 129, 128, True, 64, torch.bfloat16),
     (2, 2, 12, 7000, 128, True, 0, torch.float16),
     (1, 3, 11, 2500, 128, False, 900, torch.bfloat16),
+    # Many key splits: the merge's batched loads over several rounds and a
+    # ragged last batch (147 splits of a one-head sequence), at both head
+    # sizes, and its 256-thread form (400 merged rows, 32 splits).
+    (1, 1, 1, 131072, 128, True, 0, torch.bfloat16),
+    (1, 1, 16, 131072, 64, False, 0, torch.float16),
+    (1, 4, 100, 20000, 128, True, 0, torch.bfloat16),
 ]
 
 
