@@ -263,9 +263,11 @@ int attn_bwd_varlen(int dtype, const void* q, exattn_strides q_strides, const vo
  * alignment): under the causal mask query i sees keys j <= i + Nk - Nq, and
  * a window counts from that position.  With Nq = Nk this is attn_fwd_ex.
  * The keys are split over several CTAs per (batch, head) when B*H alone
- * cannot fill the GPU; each split writes fp32 partial results to the
+ * would leave SMs idle long enough for splits to finish sooner (few heads,
+ * long key sequences); each split writes fp32 partial results to the
  * workspace and a second kernel merges them (the same logsumexp-weighted
- * combination the online softmax uses inside one CTA).
+ * combination the online softmax uses inside one CTA).  The split count
+ * depends only on (B, H, Nq, Nk, d), so the workspace size does too.
  *   attn_fwd_decode_workspace_size -- bytes of workspace for this shape (0
  *     when no split is needed; then workspace may be NULL); 0 also for an
  *     invalid shape.
