@@ -312,6 +312,37 @@ def test_decode_plan_sizes(lib):
     assert lib.attn_fwd_decode_workspace_size(1, 1, 1, 1000, 128) == size(2, 1, 16, 128)
 
 
+def test_decode_plan_properties(lib):
+    """Over a sweep of shapes the plan the workspace implies keeps its
+    limits: at most 512 splits (the merge's limit) and about two waves of
+    152 CTAs, every split holding at least four key tiles in the decode
+    kernel (two in the forward's) unless there is one split, and the
+    workspace exactly the partials' layout."""
+    def split_count(B, H, Nq, Nk, d):
+        rows = 16 if (Nq <= 12 and d == 128) else (Nq + 255) // 256 * 256
+        per = B * H * rows * (d * 4 + 8)
+        ws = lib.attn_fwd_decode_workspace_size(B, H, Nq, Nk, d)
+        if ws == 0:
+            return 1
+        for s in range(2, 513):
+            n = s * B * H * rows
+            if ws == (n * d * 4 + 255) // 256 * 256 + 2 * ((n * 4 + 255) // 256 * 256):
+                return s
+        raise AssertionError(f"workspace {ws} matches no split count ({per} bytes per split)")
+    for B, H in ((1, 1), (1, 3), (2, 8), (1, 40), (4, 32), (8, 64)):
+        for Nk in (1, 127, 128, 1000, 5000, 32768, 131072, 1 << 20):
+            if B * H * Nk >= 1 << 31:
+                continue
+            for Nq, d in ((1, 128), (12, 128), (13, 128), (1, 64), (300, 128)):
+                s = split_count(B, H, Nq, Nk, d)
+                nkt = (Nk + 127) // 128
+                units = B * H * ((Nq + 255) // 256 if not (Nq <= 12 and d == 128) else 1)
+                floor = 4 if (Nq <= 12 and d == 128) else 2
+                assert 1 <= s <= 512
+                assert s == 1 or units * s <= 2 * 152, (B, H, Nq, Nk, d, s)
+                assert s == 1 or -(-nkt // s) >= floor, (B, H, Nq, Nk, d, s)
+
+
 def test_host_path_rejects_bad_tensors():
     """fwd_bwd_from_host checks its host tensors before any device work."""
     import torch
