@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libexattn.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "dq.cu", "decode.cu", "noalloc.cu", "host.cu"]
+SOURCES = ["api.cu", "fwd.cu", "merge.cu", "bwd.cu", "dq.cu", "decode.cu", "noalloc.cu", "host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -19,7 +19,7 @@
 //   * the epilogue reads O^T row d of every query column from lane d, so the
 //     output rows are written with consecutive threads on consecutive d.
 // Keys are split over CTAs (as in the forward's key split) and the splits'
-// fp32 partial O and logsumexps are combined by the forward's merge kernel.
+// fp32 partial O and logsumexps are combined by the split-merge kernel (merge.cu).
 // Measured against the forward kernel's key-split path on the same GPU (B8
 // H16 Nk16384 and B4 H32 Nk32768, d = 128): 1.26x faster for Nq <= 4,
 // 1.17x at 8, 1.07-1.10x at 12, slower at 16 (the per-key column work
