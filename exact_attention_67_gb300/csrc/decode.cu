@@ -171,6 +171,10 @@ __global__ void __launch_bounds__(DecThreads<T>::value, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The split merge, launched as this grid's programmatic dependent, may be
+  // scheduled once every CTA has started; it waits for this grid's completion
+  // before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, err};
 

@@ -39,6 +39,10 @@ __global__ void __launch_bounds__(THREADS) attn_merge_kernel(const float* __rest
   __shared__ float w_s[kMaxSplits];
   __shared__ float red[2][NW];
   __shared__ float acc_g[G][D];
+  // Launched as a programmatic dependent of the kernel that wrote the
+  // partials: wait until that grid has completed and its writes are visible
+  // (without such a launch this returns at once).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bh = static_cast<int>(blockIdx.x) / N, row = static_cast<int>(blockIdx.x) % N;
   const int hh = bh % H, bb = bh / H;
@@ -139,15 +143,26 @@ static cudaError_t launch_merge_t(const FwdArgs& a, cudaStream_t stream) {
   const cudaError_t e =
       note_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, a.device), "cudaDeviceGetAttribute");
   if (e != cudaSuccess) return e;
-  if (rows < 2ll * sms && a.kv.n_splits > 16) {
-    attn_merge_kernel<T, D, 1024, 16><<<static_cast<unsigned>(rows), 1024, 0, stream>>>(
-        a.kv.part_o, a.kv.part_lse, a.kv.part_lseb, a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH,
-        static_cast<T*>(a.o), a.so, a.lse);
-  } else {
-    attn_merge_kernel<T, D, 256, 4><<<static_cast<unsigned>(rows), 256, 0, stream>>>(
-        a.kv.part_o, a.kv.part_lse, a.kv.part_lseb, a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH,
-        static_cast<T*>(a.o), a.so, a.lse);
-  }
+  // A programmatic dependent launch: the blocks can be resident (waiting in
+  // griddepcontrol.wait) when the partials' last writer finishes, which
+  // hides this launch's latency behind it.
+  const bool wide = rows < 2ll * sms && a.kv.n_splits > 16;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(wide ? 1024 : 256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t le =
+      wide ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<T, D, 1024, 16>, a.kv.part_o, a.kv.part_lse, a.kv.part_lseb,
+                                a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH, static_cast<T*>(a.o), a.so, a.lse)
+           : cudaLaunchKernelEx(&cfg, attn_merge_kernel<T, D, 256, 4>, a.kv.part_o, a.kv.part_lse, a.kv.part_lseb,
+                                a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH, static_cast<T*>(a.o), a.so, a.lse);
+  if (le != cudaSuccess) return note_cuda(le, "split-merge kernel launch");
   return note_cuda(cudaGetLastError(), "split-merge kernel launch");
 }
 
