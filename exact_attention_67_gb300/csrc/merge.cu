@@ -162,8 +162,8 @@ static cudaError_t launch_merge_t(const FwdArgs& a, cudaStream_t stream) {
                                 a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH, static_cast<T*>(a.o), a.so, a.lse)
            : cudaLaunchKernelEx(&cfg, attn_merge_kernel<T, D, 256, 4>, a.kv.part_o, a.kv.part_lse, a.kv.part_lseb,
                                 a.kv.n_splits, a.kv.nq_pad, a.N, a.H, a.BH, static_cast<T*>(a.o), a.so, a.lse);
-  if (le != cudaSuccess) return note_cuda(le, "split-merge kernel launch");
-  return note_cuda(cudaGetLastError(), "split-merge kernel launch");
+  const cudaError_t last = cudaGetLastError();  // also clears a launch error le reported
+  return note_cuda(le != cudaSuccess ? le : last, "split-merge kernel launch");
 }
 
 cudaError_t launch_fwd_merge(const FwdArgs& a, cudaStream_t stream) {
